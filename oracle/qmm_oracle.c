@@ -1,0 +1,222 @@
+/*
+ * qmm_oracle.c -- plain, slow CPU oracle for the quantized matmul.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, calls or
+ * includes this file; only the test-suite, the smoke check and the
+ * benchmark's CPU-baseline leg use it.  It shares no code with the CUDA path.
+ *
+ * What it computes (fp64 for floating point, int64 for integers):
+ *
+ *  1. Bitstream.  Column n of a b-bit weight matrix is its own byte string of
+ *     K*b/8 bytes starting at packed + n*K*b/8.  Code k occupies stream bits
+ *     [k*b, k*b+b); stream bit i is bit (i mod 8), LSB = 0, of byte i/8; bit
+ *     j of the code is stream bit k*b+j.  This is the "little-endian
+ *     bitstream along K" of the workloads; the pages themselves only say that
+ *     arbitrary-width codes are loaded as raw bytes and reinterpreted
+ *     (Tilus review, pith_extraction.core_discovery) and that INT4 is packed
+ *     contiguously in bytes (BitLLM sec. 4.3, Fig. 8(a)).
+ *  2. Dequantization, BitLLM Eq. (5): w = s * (q - z), with one scale s and
+ *     one zero z per group of G consecutive codes along K (BitLLM sec. 2.2,
+ *     per-group granularity).  q - z is exact in integers, then multiplied
+ *     by the fp16 scale widened exactly to fp64.
+ *  3. Matmul: y[m][n] = sum_k x[m][k] * w[n][k], fp64, k ascending.
+ *  4. W4A8 (BitLLM sec. 4.3-4.4): signed int4 weights (two's complement
+ *     nibbles, even k in the low nibble, no zero point) and int8
+ *     activations; the integer core is the dp4a identity
+ *     r + sum_i a_i*b_i accumulated per group of G into an integer; the
+ *     epilogue is y = sa[m] * sum_g ws[n][g] * acc[m][n][g] in fp64.
+ *
+ * Every function follows the definition directly: per-bit loops, no word
+ * tricks, no blocking.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <pthread.h>
+#include <unistd.h>
+
+/* ---- 1. bitstream ------------------------------------------------------- */
+
+static int stream_bit(const uint8_t *row, long i)
+{
+    return (row[i >> 3] >> (i & 7)) & 1;
+}
+
+/* Code k of one column's bitstream: bit j of the code is stream bit k*b+j. */
+int oracle_code(const uint8_t *row, long k, int bits)
+{
+    int q = 0;
+    for (int j = 0; j < bits; ++j)
+        q |= stream_bit(row, k * bits + j) << j;
+    return q;
+}
+
+/* packed [N][K*bits/8] -> codes [N][K].  Requires K*bits % 8 == 0. */
+void oracle_unpack(const uint8_t *packed, uint8_t *codes, long N, long K, int bits)
+{
+    long row_bytes = K * bits / 8;
+    for (long n = 0; n < N; ++n)
+        for (long k = 0; k < K; ++k)
+            codes[n * K + k] = (uint8_t)oracle_code(packed + n * row_bytes, k, bits);
+}
+
+/* codes [N][K] -> packed [N][K*bits/8].  Only the low `bits` bits of each
+ * code are stored; returns how many codes had bits set at or above `bits`. */
+long oracle_pack(const uint8_t *codes, uint8_t *packed, long N, long K, int bits)
+{
+    long row_bytes = K * bits / 8;
+    long bad = 0;
+    memset(packed, 0, (size_t)(N * row_bytes));
+    for (long n = 0; n < N; ++n) {
+        uint8_t *row = packed + n * row_bytes;
+        for (long k = 0; k < K; ++k) {
+            int q = codes[n * K + k];
+            if (q >> bits)
+                ++bad;
+            for (int j = 0; j < bits; ++j) {
+                long i = k * bits + j;
+                row[i >> 3] |= (uint8_t)(((q >> j) & 1) << (i & 7));
+            }
+        }
+    }
+    return bad;
+}
+
+/* ---- thread helper: split columns n over workers -------------------------- */
+
+typedef void (*col_fn)(void *ctx, long n0, long n1);
+typedef struct { col_fn fn; void *ctx; long n0, n1; } work_t;
+
+static void *run_work(void *p)
+{
+    work_t *w = (work_t *)p;
+    w->fn(w->ctx, w->n0, w->n1);
+    return NULL;
+}
+
+static int resolve_threads(int nthreads, long N)
+{
+    if (nthreads <= 0) {
+        long c = sysconf(_SC_NPROCESSORS_ONLN);
+        nthreads = c > 0 ? (int)c : 1;
+    }
+    if (nthreads > N) nthreads = (int)(N > 0 ? N : 1);
+    if (nthreads > 256) nthreads = 256;
+    return nthreads;
+}
+
+static void parallel_columns(col_fn fn, void *ctx, long N, int nthreads)
+{
+    int T = resolve_threads(nthreads, N);
+    if (T <= 1) { fn(ctx, 0, N); return; }
+    pthread_t th[256];
+    work_t w[256];
+    for (int t = 0; t < T; ++t) {
+        w[t].fn = fn; w[t].ctx = ctx;
+        w[t].n0 = N * t / T; w[t].n1 = N * (t + 1) / T;
+        pthread_create(&th[t], NULL, run_work, &w[t]);
+    }
+    for (int t = 0; t < T; ++t) pthread_join(th[t], NULL);
+}
+
+int oracle_threads(int nthreads, long N) { return resolve_threads(nthreads, N); }
+
+/* ---- 2 + 3. dequantize, then matmul in fp64 ----------------------------------- */
+
+typedef struct {
+    const double *x; const uint8_t *packed; int bits; int group;
+    const double *scales; const uint8_t *zeros; int zero_const;
+    double *y; long M, N, K;
+} qmm_ctx;
+
+static void qmm_cols(void *p, long n0, long n1)
+{
+    qmm_ctx *c = (qmm_ctx *)p;
+    long K = c->K, ng = K / c->group, row_bytes = K * c->bits / 8;
+    double *w = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+    for (long n = n0; n < n1; ++n) {
+        const uint8_t *row = c->packed + n * row_bytes;
+        for (long k = 0; k < K; ++k) {
+            long g = k / c->group;
+            long q = oracle_code(row, k, c->bits);
+            long z = c->zeros ? c->zeros[n * ng + g] : c->zero_const;
+            w[k] = (double)(q - z) * c->scales[n * ng + g];      /* Eq. (5) */
+        }
+        for (long m = 0; m < c->M; ++m) {
+            double acc = 0.0;
+            for (long k = 0; k < K; ++k)
+                acc += c->x[m * K + k] * w[k];
+            c->y[m * c->N + n] = acc;
+        }
+    }
+    free(w);
+}
+
+/* y[M][N] = x[M][K] . W^T with W[n][k] = (q[n][k] - z[n][k/G]) * s[n][k/G].
+ * x and scales are the stored fp16/bf16 values widened exactly to fp64;
+ * zeros is [N][K/G] uint8 or NULL (then zero_const is used). */
+void oracle_qmm(const double *x, const uint8_t *packed, int bits, int group,
+                const double *scales, const uint8_t *zeros, int zero_const,
+                double *y, long M, long N, long K, int nthreads)
+{
+    qmm_ctx c = { x, packed, bits, group, scales, zeros, zero_const, y, M, N, K };
+    parallel_columns(qmm_cols, &c, N, nthreads);
+}
+
+/* ---- 4. W4A8 integer core and epilogue ---------------------------------------- */
+
+/* Two's-complement value of a 4-bit code. */
+int oracle_int4_value(int code)
+{
+    return (code & 8) ? (code & 15) - 16 : (code & 15);
+}
+
+/* The dot-product primitive: r + sum_i a[i]*b[i] with int8 inputs and a wide
+ * integer accumulator (dp4a is the n = 4 case). */
+int64_t oracle_dot_i8(const int8_t *a, const int8_t *b, long n, int64_t r)
+{
+    for (long i = 0; i < n; ++i)
+        r += (int64_t)a[i] * (int64_t)b[i];
+    return r;
+}
+
+typedef struct {
+    const int8_t *xq; const double *sa; const uint8_t *w4; const double *ws;
+    int group; int64_t *acc; double *y; long M, N, K; int overflow;
+} w4a8_ctx;
+
+static void w4a8_cols(void *p, long n0, long n1)
+{
+    w4a8_ctx *c = (w4a8_ctx *)p;
+    long K = c->K, ng = K / c->group, row_bytes = K / 2;
+    int8_t *w = (int8_t *)malloc((size_t)(K > 0 ? K : 1));
+    for (long n = n0; n < n1; ++n) {
+        const uint8_t *row = c->w4 + n * row_bytes;
+        for (long k = 0; k < K; ++k)
+            w[k] = (int8_t)oracle_int4_value(oracle_code(row, k, 4));
+        for (long m = 0; m < c->M; ++m) {
+            double yy = 0.0;
+            for (long g = 0; g < ng; ++g) {
+                int64_t a = oracle_dot_i8(c->xq + m * K + g * c->group,
+                                          w + g * c->group, c->group, 0);
+                if (a > INT32_MAX || a < INT32_MIN) c->overflow = 1;
+                if (c->acc) c->acc[(m * c->N + n) * ng + g] = a;
+                yy += c->ws[n * ng + g] * (double)a;
+            }
+            c->y[m * c->N + n] = c->sa[m] * yy;
+        }
+    }
+    free(w);
+}
+
+/* acc[m][n][g] = sum_{k in g} xq[m][k] * w4[n][k]   (int64, may be NULL)
+ * y[m][n]      = sa[m] * sum_g ws[n][g] * acc[m][n][g]   (fp64)
+ * Returns 1 if any accumulator falls outside the int32 range, else 0. */
+int oracle_w4a8(const int8_t *xq, const double *sa, const uint8_t *w4,
+                const double *ws, int group, int64_t *acc, double *y,
+                long M, long N, long K, int nthreads)
+{
+    w4a8_ctx c = { xq, sa, w4, ws, group, acc, y, M, N, K, 0 };
+    parallel_columns(w4a8_cols, &c, N, nthreads);
+    return c.overflow;
+}

@@ -1,0 +1,254 @@
+"""Pins for the CPU oracle, independent of the oracle's own code.
+
+Each check ties the oracle to something other than itself: hand-derived
+packed bytes (tests/golden), the INT8 dot product printed in BitLLM Fig. 2(c),
+Python big-integer bit extraction (a different idiom from the oracle's per-bit
+loop), exact rational brute force, a special case that reduces to a library
+matmul, and closed forms.  They are chosen so that a dropped term, a wrong
+sign, a wrong index or a transposed operand in the oracle fails at least one.
+"""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from synthetic import SplitMix64
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                yield [p.strip() for p in line.split("|")]
+
+
+def _bigint_pack(codes_row, bits):
+    """Independent packer: build one Python integer, write it little-endian."""
+    v = 0
+    for k, q in enumerate(codes_row):
+        v |= int(q) << (k * bits)
+    return np.frombuffer(v.to_bytes(len(codes_row) * bits // 8, "little"), dtype=np.uint8)
+
+
+def _bigint_codes(row_bytes, K, bits):
+    v = int.from_bytes(bytes(row_bytes), "little")
+    return [(v >> (k * bits)) & ((1 << bits) - 1) for k in range(K)]
+
+
+# ---- bitstream -----------------------------------------------------------------
+@pytest.mark.parametrize("case", list(_golden_lines("bitstream_examples.txt")))
+def test_hand_packed_examples(case):
+    bits = int(case[0])
+    codes = np.array([int(t) for t in case[1].split()], dtype=np.uint8)[None, :]
+    expect = np.array([int(t, 16) for t in case[2].split()], dtype=np.uint8)[None, :]
+    packed, bad = oracle.pack(codes, bits)
+    assert bad == 0
+    np.testing.assert_array_equal(packed, expect)
+    np.testing.assert_array_equal(oracle.unpack(expect, codes.shape[1], bits), codes)
+    for k in range(codes.shape[1]):
+        assert oracle.code_at(expect[0], k, bits) == codes[0, k]
+
+
+def test_golden_signed_int4_values():
+    # the last golden line holds the weights -8 7 -1 0 3 -5 1 -2 as codes
+    codes = [8, 7, 15, 0, 3, 11, 1, 14]
+    assert [oracle.int4_value(c) for c in codes] == [-8, 7, -1, 0, 3, -5, 1, -2]
+
+
+@pytest.mark.parametrize("bits", range(1, 9))
+@pytest.mark.parametrize("K", [8, 24, 40, 256, 1000])
+def test_roundtrip_codes(bits, K):
+    if (K * bits) % 8:
+        pytest.skip("K*bits must be byte aligned")
+    st = SplitMix64(bits * 1000 + K)
+    codes = st.uniform_bits(3 * K, bits).reshape(3, K)
+    packed, bad = oracle.pack(codes, bits)
+    assert bad == 0
+    assert packed.shape == (3, K * bits // 8)
+    np.testing.assert_array_equal(oracle.unpack(packed, K, bits), codes)
+
+
+@pytest.mark.parametrize("bits", range(1, 9))
+def test_roundtrip_bytes_is_bijection(bits):
+    K = 64
+    st = SplitMix64(77 + bits)
+    raw = st.uniform_bits(5 * K * bits // 8, 8).reshape(5, K * bits // 8)
+    codes = oracle.unpack(raw, K, bits)
+    assert codes.max() < (1 << bits)
+    again, _ = oracle.pack(codes, bits)
+    np.testing.assert_array_equal(again, raw)
+
+
+@pytest.mark.parametrize("bits", range(1, 9))
+def test_bigint_idiom_agrees(bits):
+    K, N = 96, 4
+    st = SplitMix64(500 + bits)
+    codes = st.uniform_bits(N * K, bits).reshape(N, K)
+    packed, _ = oracle.pack(codes, bits)
+    for n in range(N):
+        np.testing.assert_array_equal(packed[n], _bigint_pack(codes[n], bits))
+        assert _bigint_codes(packed[n], K, bits) == list(codes[n])
+
+
+def test_view_bit_conservation():
+    # eight b-bit codes fill exactly b bytes (u8[3] <-> i6[4] is the b=6 case:
+    # four 6-bit codes in three bytes)
+    for bits in range(1, 9):
+        packed, _ = oracle.pack(np.zeros((1, 8), np.uint8), bits)
+        assert packed.shape[1] == bits
+    packed, _ = oracle.pack(np.array([[63, 0, 63, 0]], np.uint8), 6)
+    assert packed.shape == (1, 3)
+    np.testing.assert_array_equal(packed[0], [0x3F, 0xF0, 0x03])
+
+
+def test_width8_identity_and_width4_nibbles():
+    st = SplitMix64(9)
+    c8 = st.uniform_bits(3 * 40, 8).reshape(3, 40)
+    np.testing.assert_array_equal(oracle.pack(c8, 8)[0], c8)
+    c4 = st.uniform_bits(3 * 40, 4).reshape(3, 40)
+    p4 = oracle.pack(c4, 4)[0]
+    np.testing.assert_array_equal(p4, c4[:, 0::2] | (c4[:, 1::2] << 4))
+
+
+def test_pack_counts_and_truncates_out_of_range():
+    codes = np.array([[0, 5, 8, 15, 16, 255, 3, 9]], np.uint8)
+    packed, bad = oracle.pack(codes, 3)
+    assert bad == 5  # 8, 15, 16, 255 and 9 do not fit in 3 bits
+    np.testing.assert_array_equal(oracle.unpack(packed, 8, 3), codes & 7)
+
+
+def test_columns_are_independent_streams():
+    st = SplitMix64(11)
+    for bits in (3, 5, 7):
+        K = 40
+        codes = st.uniform_bits(3 * K, bits).reshape(3, K)
+        packed, _ = oracle.pack(codes, bits)
+        for n in range(3):
+            np.testing.assert_array_equal(packed[n], oracle.pack(codes[n:n + 1], bits)[0][0])
+
+
+# ---- dequantize + matmul ---------------------------------------------------------
+def _dyadic_fp16(st, n, den_bits, lo, hi):
+    """Random dyadic values p / 2**den_bits, exactly representable in fp16."""
+    span = hi - lo + 1
+    raw = (st.next(n) % np.uint64(span)).astype(np.int64) + lo
+    return (raw.astype(np.float64) / (1 << den_bits)).astype(np.float16)
+
+
+@pytest.mark.parametrize("bits", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("zero_mode", ["const", "group"])
+def test_qmm_brute_force_exact(bits, zero_mode):
+    st = SplitMix64(1234 + bits)
+    M, N, K, G = 3, 5, 64, 32
+    codes = st.uniform_bits(N * K, bits).reshape(N, K)
+    scales = _dyadic_fp16(st, N * (K // G), 6, 1, 63).reshape(N, K // G)
+    x = _dyadic_fp16(st, M * K, 4, -64, 64).reshape(M, K)
+    zc = (1 << bits) // 2 + 1 if bits > 1 else 1
+    zeros = st.uniform_bits(N * (K // G), bits).reshape(N, K // G) if zero_mode == "group" else None
+    packed = np.stack([_bigint_pack(codes[n], bits) for n in range(N)])
+    y = oracle.qmm(x.astype(np.float64), packed, bits, G, scales.astype(np.float64),
+                   zeros, zc, K, nthreads=2)
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                z = int(zeros[n, k // G]) if zeros is not None else zc
+                w = (int(codes[n, k]) - z) * Fraction(float(scales[n, k // G]))
+                acc += Fraction(float(x[m, k])) * w
+            assert y[m, n] == float(acc), (m, n)
+
+
+def test_qmm_reduces_to_library_matmul():
+    # s = 1, z = 0, b = 8: W is the code matrix itself, y = x . Q^T
+    st = SplitMix64(42)
+    M, N, K = 4, 7, 256
+    codes = st.uniform_bits(N * K, 8).reshape(N, K)
+    x = st.normal(M * K).reshape(M, K).astype(np.float16).astype(np.float64)
+    packed, _ = oracle.pack(codes, 8)
+    y = oracle.qmm(x, packed, 8, 128, np.ones((N, K // 128)), None, 0, K)
+    ref = x @ codes.astype(np.float64).T
+    np.testing.assert_allclose(y, ref, rtol=1e-13, atol=1e-10)
+
+
+@pytest.mark.parametrize("bits", [1, 4, 6])
+def test_qmm_all_ones_closed_form(bits):
+    st = SplitMix64(7 + bits)
+    N, K, G = 6, 256, 64
+    codes = st.uniform_bits(N * K, bits).reshape(N, K)
+    zeros = st.uniform_bits(N * (K // G), bits).reshape(N, K // G)
+    scales = (0.02 * np.abs(st.normal(N * (K // G))) + 1e-3).astype(np.float16).reshape(N, K // G)
+    packed, _ = oracle.pack(codes, bits)
+    y = oracle.qmm(np.ones((1, K)), packed, bits, G, scales.astype(np.float64), zeros, 0, K)
+    for n in range(N):
+        expect = sum(float(scales[n, g]) * sum(int(codes[n, k]) - int(zeros[n, g])
+                                               for k in range(g * G, (g + 1) * G))
+                     for g in range(K // G))
+        assert abs(y[0, n] - expect) <= 1e-12 * max(1.0, abs(expect))
+
+
+def test_qmm_thread_count_does_not_change_result():
+    st = SplitMix64(3)
+    M, N, K = 2, 33, 512
+    codes = st.uniform_bits(N * K, 5).reshape(N, K)
+    packed, _ = oracle.pack(codes, 5)
+    x = st.normal(M * K).reshape(M, K)
+    s = np.abs(st.normal(N * 4)).reshape(N, 4)
+    a = oracle.qmm(x, packed, 5, 128, s, None, 16, K, nthreads=1)
+    b = oracle.qmm(x, packed, 5, 128, s, None, 16, K, nthreads=5)
+    np.testing.assert_array_equal(a, b)
+
+
+# ---- W4A8 integer core -------------------------------------------------------------
+@pytest.mark.parametrize("case", list(_golden_lines("int8_dot_example.txt")))
+def test_int8_dot_printed_example(case):
+    a = np.array([int(t) for t in case[0].split()], np.int8)
+    b = np.array([int(t) for t in case[1].split()], np.int8)
+    assert oracle.dot_i8(a, b, int(case[2])) == int(case[3])
+
+
+def test_dp4a_identity_brute_force():
+    st = SplitMix64(99)
+    for _ in range(50):
+        a = st.uniform_int8_sym(4)
+        b = st.uniform_int8_sym(4)
+        r = int(st.next(1)[0] >> np.uint64(40)) - (1 << 23)
+        assert oracle.dot_i8(a, b, r) == r + sum(int(u) * int(v) for u, v in zip(a, b))
+
+
+def test_w4a8_brute_force_exact():
+    st = SplitMix64(5)
+    M, N, K, G = 3, 4, 256, 128
+    w4 = st.uniform_bits(N * K, 4).reshape(N, K)
+    xq = st.uniform_int8_sym(M * K).reshape(M, K)
+    ws = _dyadic_fp16(st, N * (K // G), 8, 1, 200).reshape(N, K // G)
+    sa = _dyadic_fp16(st, M, 8, 1, 200)
+    packed = np.stack([_bigint_pack(w4[n], 4) for n in range(N)])
+    y, acc, ov = oracle.w4a8(xq, sa.astype(np.float64), packed, ws.astype(np.float64), G, K)
+    assert not ov
+    for m in range(M):
+        for n in range(N):
+            tot = Fraction(0)
+            for g in range(K // G):
+                a = 0
+                for k in range(g * G, (g + 1) * G):
+                    c = int(w4[n, k])
+                    a += int(xq[m, k]) * (c - 16 if c >= 8 else c)
+                assert acc[m, n, g] == a
+                tot += Fraction(float(ws[n, g])) * a
+            assert y[m, n] == float(Fraction(float(sa[m])) * tot)
+
+
+def test_w4a8_extreme_accumulator_fits_int32():
+    K, G = 256, 128
+    xq = np.full((1, K), -127, np.int8)
+    w4 = np.full((1, K), 8, np.uint8)  # -8
+    packed, _ = oracle.pack(w4, 4)
+    y, acc, ov = oracle.w4a8(xq, np.ones(1), packed, np.ones((1, 2)), G, K)
+    assert not ov
+    assert (acc == 127 * 8 * G).all()
+    assert y[0, 0] == 2 * 127 * 8 * G
