@@ -1,0 +1,188 @@
+"""FP16/BF16 x INT1-8 quantized matmul on GB300 (sm_103a).
+
+A thin ctypes binding over ``lib/libqmm.so`` (C ABI in ``include/qmm.h``).
+The functions keep the C names and only marshal arguments: torch tensors are
+used for device memory and the current CUDA stream, every step of the
+computation runs in the library's kernels.  There is no CPU fallback: if the
+library has not been built (``python -m bit_weight_quantized_gb300.build``) or
+no sm_103a device is present, calls raise.
+
+Storage: the b-bit weight matrix is a per-column LSB-first bitstream along K,
+``packed[n]`` holding K*b/8 bytes (see qmm.h); scales are fp16 ``[N][K/G]``,
+zeros are uint8 ``[N][K/G]`` or a constant.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libqmm.so")
+
+QMM_F16 = 0
+QMM_BF16 = 1
+
+STATUS_NAMES = {
+    0: "QMM_OK", 1: "QMM_ERR_NULL", 2: "QMM_ERR_BITS", 3: "QMM_ERR_SHAPE",
+    4: "QMM_ERR_ALIGN", 5: "QMM_ERR_UNSUPPORTED", 6: "QMM_ERR_CUDA",
+    8: "QMM_ERR_TIMEOUT", 9: "QMM_ERR_DEVICE",
+}
+
+# C entry points and their ctypes signatures (must match include/qmm.h)
+_P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "qmm_pack": ([_P, _P, _I, _I, _I, _P, _P], _I),
+    "qmm_unpack": ([_P, _P, _I, _I, _I, _P], _I),
+    "qmm_gemv": ([_P, _I, _P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P], _I),
+    "qmm_gemm": ([_P, _I, _P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P], _I),
+    "qmm_w4a8": ([_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P], _I),
+    "qmm_device_status": ([_P], _I),
+    "qmm_status_string": ([_I], ctypes.c_char_p),
+    "qmm_abi_version": ([], _I),
+}
+
+_lib = None
+
+
+class QmmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libqmm.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise ImportError(f"libqmm.so not built ({path}); run "
+                              "`python -m bit_weight_quantized_gb300.build`")
+        lib = ctypes.CDLL(path)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+    return _lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise QmmError(status, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device=None):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+_DT = {torch.float16: QMM_F16, torch.bfloat16: QMM_BF16}
+
+
+def qmm_pack(codes: torch.Tensor, bits: int, bad_count: Optional[torch.Tensor] = None,
+             out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """uint8 codes [N][K] -> packed bitstream [N][K*bits/8] (see qmm_pack)."""
+    _dev(codes, "codes", torch.uint8)
+    N, K = codes.shape
+    if out is None:
+        out = torch.empty((N, K * bits // 8), dtype=torch.uint8, device=codes.device)
+    if bad_count is not None:
+        _dev(bad_count, "bad_count", torch.int32)
+    _check(load().qmm_pack(_ptr(codes), _ptr(out), N, K, bits, _ptr(bad_count),
+                           _stream(codes.device)), "qmm_pack")
+    return out
+
+
+def qmm_unpack(packed: torch.Tensor, K: int, bits: int) -> torch.Tensor:
+    _dev(packed, "packed", torch.uint8)
+    N = packed.shape[0]
+    out = torch.empty((N, K), dtype=torch.uint8, device=packed.device)
+    _check(load().qmm_unpack(_ptr(packed), _ptr(out), N, K, bits, _stream(packed.device)),
+           "qmm_unpack")
+    return out
+
+
+def _qmm(name, x, packed, bits, group, scales, zeros, zero_const, out, out_dtype):
+    _dev(x, "x")
+    M, K = x.shape
+    _dev(packed, "packed", torch.uint8)
+    N = packed.shape[0]
+    if packed.shape[1] * 8 != K * bits:
+        raise ValueError("packed must be [N][K*bits/8]")
+    _dev(scales, "scales", torch.float16, (N, K // group))
+    if zeros is not None:
+        _dev(zeros, "zeros", torch.uint8, (N, K // group))
+    if x.dtype not in _DT:
+        raise ValueError("x must be float16 or bfloat16")
+    out_dtype = out_dtype or x.dtype
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    _dev(out, "out", out_dtype, (M, N))
+    fn = getattr(load(), name)
+    _check(fn(_ptr(x), _DT[x.dtype], _ptr(packed), bits, group, _ptr(scales), _ptr(zeros),
+              int(zero_const), _ptr(out), _DT[out_dtype], M, N, K, _stream(x.device)), name)
+    return out
+
+
+def qmm_gemv(x, packed, bits, group, scales, zeros=None, zero_const=0, out=None,
+             out_dtype=None) -> torch.Tensor:
+    """y[M][N] = x . W^T for 1 <= M <= 16 (decode / skinny)."""
+    return _qmm("qmm_gemv", x, packed, bits, group, scales, zeros, zero_const, out, out_dtype)
+
+
+def qmm_gemm(x, packed, bits, group, scales, zeros=None, zero_const=0, out=None,
+             out_dtype=None) -> torch.Tensor:
+    """y[M][N] = x . W^T for M >= 17 (tiled tensor-core path)."""
+    return _qmm("qmm_gemm", x, packed, bits, group, scales, zeros, zero_const, out, out_dtype)
+
+
+def qmm_w4a8(xq, sa, w4, ws, group=128, want_acc=False, out=None, acc_out=None):
+    """Integer-native W4A8: returns y (fp16 [M][N]) and, if requested, the int32
+    accumulators [M][N][K/group]."""
+    _dev(xq, "xq", torch.int8)
+    M, K = xq.shape
+    _dev(sa, "sa", torch.float16, (M,))
+    _dev(w4, "w4", torch.uint8)
+    N = w4.shape[0]
+    if w4.shape[1] * 2 != K:
+        raise ValueError("w4 must be [N][K/2]")
+    _dev(ws, "ws", torch.float16, (N, K // group))
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=xq.device)
+    if want_acc and acc_out is None:
+        acc_out = torch.empty((M, N, K // group), dtype=torch.int32, device=xq.device)
+    _check(load().qmm_w4a8(_ptr(xq), _ptr(sa), _ptr(w4), _ptr(ws), group, _ptr(out),
+                           _ptr(acc_out), M, N, K, _stream(xq.device)), "qmm_w4a8")
+    return (out, acc_out) if want_acc else out
+
+
+def qmm_device_status(stream=None) -> int:
+    """Synchronizes the stream and returns (and clears) the device status word."""
+    s = ctypes.c_void_p(stream.cuda_stream) if stream is not None else _stream()
+    return load().qmm_device_status(s)
+
+
+def qmm_status_string(status: int) -> str:
+    return load().qmm_status_string(status).decode()
+
+
+def native_library_path() -> str:
+    return LIB_PATH

@@ -1,0 +1,88 @@
+// pack.cu -- b-bit codes <-> per-column LSB-first bitstream (offline step).
+//
+// Column n's stream is K*b/8 bytes; code k occupies stream bits [k*b, k*b+b)
+// and stream bit i is bit (i mod 8) of byte i/8.  Packing is not on the timed
+// decode path, so these kernels favour simplicity: one thread per output
+// byte (pack) or per code (unpack).
+#include "common.cuh"
+
+namespace qmm {
+
+__global__ void pack_kernel(const uint8_t *__restrict__ codes, uint8_t *__restrict__ packed,
+                            long long N, long long K, int bits, int32_t *bad_count)
+{
+    const long long row_bytes = K * bits / 8;
+    const long long total = N * row_bytes;
+    const int mask = (1 << bits) - 1;
+    int bad = 0;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long n = idx / row_bytes;
+        const long long j = idx - n * row_bytes;        // byte within the row
+        const long long bit0 = 8 * j;                   // first stream bit of this byte
+        const long long k0 = bit0 / bits;
+        const long long k1 = (bit0 + 7) / bits;         // last code touching the byte
+        const uint8_t *row = codes + n * K;
+        uint32_t out = 0;
+        for (long long k = k0; k <= k1 && k < K; ++k) {
+            const int q = row[k];
+            const long long sh = k * bits - bit0;       // in [-7, 7]
+            const uint32_t v = static_cast<uint32_t>(q & mask);
+            out |= sh >= 0 ? (v << sh) : (v >> (-sh));
+            if (k * bits >= bit0 && (q & ~mask))        // count each code once, at its first byte
+                ++bad;
+        }
+        packed[idx] = static_cast<uint8_t>(out & 0xFF);
+    }
+    if (bad_count) {
+        // one atomic per warp
+        for (int o = 16; o > 0; o >>= 1)
+            bad += __shfl_xor_sync(0xffffffffu, bad, o);
+        if ((threadIdx.x & 31) == 0 && bad)
+            atomicAdd(bad_count, bad);
+    }
+}
+
+__global__ void unpack_kernel(const uint8_t *__restrict__ packed, uint8_t *__restrict__ codes,
+                              long long N, long long K, int bits)
+{
+    const long long row_bytes = K * bits / 8;
+    const long long total = N * K;
+    const int mask = (1 << bits) - 1;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long n = idx / K;
+        const long long k = idx - n * K;
+        const uint8_t *row = packed + n * row_bytes;
+        const long long b0 = k * bits;
+        const long long byte = b0 >> 3;
+        uint32_t v = row[byte];
+        if (byte + 1 < row_bytes)
+            v |= static_cast<uint32_t>(row[byte + 1]) << 8;
+        codes[idx] = static_cast<uint8_t>((v >> (b0 & 7)) & mask);
+    }
+}
+
+cudaError_t launch_pack(const uint8_t *codes, uint8_t *packed, int N, int K, int bits,
+                        int32_t *bad_count, cudaStream_t stream, int num_sms)
+{
+    const long long total = (long long)N * K * bits / 8;
+    long long blocks = (total + 255) / 256;
+    if (blocks > (long long)num_sms * 16)
+        blocks = (long long)num_sms * 16;
+    pack_kernel<<<(int)blocks, 256, 0, stream>>>(codes, packed, N, K, bits, bad_count);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unpack(const uint8_t *packed, uint8_t *codes, int N, int K, int bits,
+                          cudaStream_t stream, int num_sms)
+{
+    const long long total = (long long)N * K;
+    long long blocks = (total + 255) / 256;
+    if (blocks > (long long)num_sms * 16)
+        blocks = (long long)num_sms * 16;
+    unpack_kernel<<<(int)blocks, 256, 0, stream>>>(packed, codes, N, K, bits);
+    return cudaGetLastError();
+}
+
+}  // namespace qmm

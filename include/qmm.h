@@ -1,0 +1,149 @@
+/*
+ * qmm.h -- C ABI of libqmm: FP16/BF16 activations x b-bit quantized weights
+ * (b = 1..8), and the integer-native W4A8 variant, on one GB300 (sm_103a).
+ *
+ * The operation (Tilus review, lead and pith_extraction.core_discovery: a
+ * matmul of FP16 activations by weights of any width from 1 to 8 bits that
+ * are loaded as packed bytes and reinterpreted; BitLLM sec. 2.2 Eq. (5) and
+ * sec. 4.3-4.4 for the per-group affine dequantization and the int8 x int4
+ * integer pipeline):
+ *
+ *     y[m][n] = sum_k x[m][k] * W[n][k],
+ *     W[n][k] = (q[n][k] - z[n][k/G]) * s[n][k/G]          (BitLLM Eq. 5)
+ *
+ * Weight storage ("packed bitstream"): column n (output feature n) is its
+ * own byte string of K*b/8 bytes at packed + n*K*b/8.  Code k occupies
+ * stream bits [k*b, k*b+b); stream bit i is bit (i mod 8) of byte i/8
+ * (LSB first); bit j of the code is stream bit k*b+j.  So 8 codes always
+ * fill exactly b bytes, and a group of 32 codes is exactly b 32-bit words.
+ *
+ * Conventions for every call:
+ *  - Pointers marked (device) are device memory owned by the caller; the
+ *    library allocates nothing and keeps no per-call state.  Pointers marked
+ *    (host) are host memory.
+ *  - fp16 / bf16 tensors are passed as void* holding 16-bit IEEE binary16 /
+ *    bfloat16 bit patterns.  Matrices are dense and row-major with the
+ *    shapes given; there are no stride arguments.
+ *  - Every call is asynchronous on `stream` (0 = the legacy default
+ *    stream).  Argument errors are detected on the host before anything is
+ *    launched and return a status without touching the device.  Launch
+ *    failures return QMM_ERR_CUDA.  Device-side watchdog expiries (a
+ *    pipeline wait that did not complete within about a second) do not trap:
+ *    the kernel records QMM_ERR_TIMEOUT in a device status word, leaves its
+ *    outputs unspecified and returns; qmm_device_status() reports and clears
+ *    it.  Nothing in the library aborts, throws across the ABI or traps.
+ *  - Outputs are written with round-to-nearest-even from fp32.
+ */
+#ifndef QMM_H_
+#define QMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define QMM_API __attribute__((visibility("default")))
+#else
+#define QMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QMM_OK = 0,
+    QMM_ERR_NULL = 1,         /* a required pointer is NULL                      */
+    QMM_ERR_BITS = 2,         /* bits outside the supported range               */
+    QMM_ERR_SHAPE = 3,        /* negative size, K % group, unsupported M range  */
+    QMM_ERR_ALIGN = 4,        /* a pointer or row pitch breaks an alignment rule */
+    QMM_ERR_UNSUPPORTED = 5,  /* valid but not implemented (dtype, group, size) */
+    QMM_ERR_CUDA = 6,         /* a CUDA runtime call or kernel launch failed     */
+    QMM_ERR_TIMEOUT = 8,      /* device watchdog expired (see qmm_device_status) */
+    QMM_ERR_DEVICE = 9        /* no usable sm_103a device                       */
+} qmm_status;
+
+typedef enum { QMM_F16 = 0, QMM_BF16 = 1 } qmm_dtype;
+
+/* Pack b-bit codes into the column bitstream (packing is the storage format
+ * above; BitLLM sec. 4.3 Fig. 8(a) is the b = 4 case).
+ *   codes     (device) uint8 [N][K]; only the low `bits` bits of each code are
+ *             stored.
+ *   packed    (device) uint8 [N][K*bits/8], fully overwritten.
+ *   bad_count (device, may be NULL) int32; the number of codes >= 2^bits is
+ *             ADDED to it (the caller zeroes it first if a fresh count is
+ *             wanted).
+ * Requires 1 <= bits <= 8, N >= 0, K >= 0, K*bits % 8 == 0. */
+QMM_API qmm_status qmm_pack(const uint8_t *codes, uint8_t *packed, int N, int K, int bits,
+                    int32_t *bad_count, cudaStream_t stream);
+
+/* Inverse of qmm_pack (a test aid): packed (device) [N][K*bits/8] ->
+ * codes (device) uint8 [N][K]. */
+QMM_API qmm_status qmm_unpack(const uint8_t *packed, uint8_t *codes, int N, int K, int bits,
+                      cudaStream_t stream);
+
+/* Decode / skinny matmul, 1 <= M <= 16 (BitLLM sec. 5.1 decodes at batch 1;
+ * the skinny range covers small batches).  Streams the bitstream through
+ * shared memory with TMA, extracts codes in registers and accumulates in
+ * fp32 on tensor cores.
+ *   x        (device) [M][K] activations, dtype x_dtype (QMM_F16 only).
+ *   packed   (device) [N][K*bits/8] bitstream, 16-byte aligned.
+ *   bits     1..8.   group: G in {32, 64, 128}, K % G == 0.
+ *   scales   (device) fp16 [N][K/G].
+ *   zeros    (device) uint8 [N][K/G], or NULL to use zero_const for every
+ *            group (0 <= zero_const <= 255).
+ *   y        (device) [M][N], dtype y_dtype (QMM_F16 or QMM_BF16).
+ * The tensor cores see the integer codes q exactly (as fp16) and the fp16
+ * activations, and accumulate each group in fp32; the group's scale and zero
+ * are applied in fp32 afterwards as s*(sum q*x - z*sum x), which equals
+ * sum s*(q - z)*x.  Results are deterministic run to run.
+ * Activations of M x K fp16 must fit in shared memory next to the weight
+ * pipeline (M*K <= 64K elements for M <= 8 and K = 4096 class shapes; larger
+ * return QMM_ERR_UNSUPPORTED).  K % 32 == 0 is implied by the group rule. */
+QMM_API qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int bits,
+                    int group, const void *scales, const uint8_t *zeros, int zero_const,
+                    void *y, qmm_dtype y_dtype, int M, int N, int K, cudaStream_t stream);
+
+/* Tiled matmul for M >= 17 (the dense-contraction regime, Tilus review
+ * supporting_citations [41]: tensor-core instruction layouts).  Same
+ * arguments and storage as qmm_gemv; activations and outputs may be
+ * QMM_BF16 or QMM_F16 (x_dtype == y_dtype).  Weights are dequantized to
+ * bf16/fp16 (q - z) * s tiles in shared memory and multiplied with
+ * tcgen05 MMAs accumulating in fp32 in tensor memory. */
+QMM_API qmm_status qmm_gemm(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int bits,
+                    int group, const void *scales, const uint8_t *zeros, int zero_const,
+                    void *y, qmm_dtype y_dtype, int M, int N, int K, cudaStream_t stream);
+
+/* Integer-native W4A8 (BitLLM sec. 4.3-4.4: int8 x int4 dot products into
+ * int32, dequantization deferred to an epilogue):
+ *   acc[m][n][g] = sum_{k in group g} xq[m][k] * w[n][k]          (int32, exact)
+ *   y[m][n]      = sa[m] * sum_g ws[n][g] * acc[m][n][g]          (fp32 -> fp16)
+ *   xq      (device) int8 [M][K] activations.
+ *   sa      (device) fp16 [M] per-token activation scales.
+ *   w4      (device) uint8 [N][K/2]: signed int4 weights in [-8, 7], 4-bit two's
+ *           complement, the b = 4 bitstream (even k in the low nibble).
+ *   ws      (device) fp16 [N][K/G] per-group weight scales, G in {32, 64, 128}.
+ *   y       (device) fp16 [M][N].
+ *   acc_out (device, may be NULL) int32 [M][N][K/G]: the integer accumulators.
+ * Requires 1 <= M <= 64 (decode and small batches), K % G == 0. */
+QMM_API qmm_status qmm_w4a8(const int8_t *xq, const void *sa, const uint8_t *w4, const void *ws,
+                    int group, void *y, int32_t *acc_out, int M, int N, int K,
+                    cudaStream_t stream);
+
+/* Synchronizes `stream`, then returns and clears the first device-side error
+ * recorded by any qmm kernel on the current device (QMM_OK if none).  A
+ * pending asynchronous CUDA error is reported as QMM_ERR_CUDA. */
+QMM_API qmm_status qmm_device_status(cudaStream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+QMM_API const char *qmm_status_string(qmm_status status);
+
+/* ABI version of this header (increases on incompatible change). */
+QMM_API int qmm_abi_version(void);
+
+#define QMM_ABI_VERSION 1
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QMM_H_ */
