@@ -1,0 +1,495 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized-matmul hot path on GB300.
+
+Workload: the decode GEMV width sweep -- M = 1, K = N = 4096 (a 7B-class
+q_proj), bits b = 1..8, group 128, zero 2^(b-1), fp16 activations and
+outputs, seeded synthetic data (synthetic.decode_sweep).  One step is one
+pass over the eight widths: eight qmm_gemv calls, each on its own packed
+weight matrix.  The metric is the effective HBM bandwidth: algorithmic bytes
+(packed weights + scales + activations + outputs, each once) per second.
+
+Timing: the step's launches are captured once in a CUDA graph per input copy
+(CPU launch overhead would otherwise dominate kernels of a few microseconds);
+the inputs rotate over copies whose total exceeds twice the L2, so every step
+reads its weights from HBM.  W warm-up steps, then exactly K timed steps
+between a barrier + synchronize on both sides, CUDA events on the launching
+stream, max over ranks.  Kernel durations for the roofline come from a second
+replay of the same launches with timing events between them.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun each rank runs its own replica of the sweep (weak scaling, no
+collective on the data path).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Quantized-matmul effective HBM GB/s (% of ~8 TB/s roofline); TFLOP/s at M≥128"
+WORKLOAD = ("decode GEMV width sweep: M=1, K=N=4096, bits 1..8, group 128, "
+            "z=2^(b-1), fp16 activations/outputs, fp32 accumulation")
+BITS = list(range(1, 9))
+PROFILE = os.path.join(ROOT, "profiles", "qmm_gemv_decode_sweep.txt")
+KERNEL_SOURCES = ["gemv.cu", "common.cuh", "unpack_plans.h"]
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha1()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "bit_weight_quantized_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def profile_traffic():
+    """ncu DRAM bytes per launch of the sweep's gemv kernels, if the committed
+    capture was taken on the current kernel source; else None."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None
+    kv = dict(line.split(":", 1) for line in text.splitlines() if ":" in line and not line.startswith(" "))
+    if kv.get("kernel_source_sha1", "").strip() != kernel_source_digest():
+        return None
+    try:
+        return float(kv["dram_bytes_per_sweep_launch_avg"].strip())
+    except (KeyError, ValueError):
+        return None
+
+
+# ---- clocks during the timed region --------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.dev)],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        for r in rows:
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                "sw_power_cap"), r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---- distributed helpers -------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("QMM_BENCH_BACKEND", "nccl")
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value: float) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(world, value: float) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---- CPU oracle leg --------------------------------------------------------------------
+class OracleSweep:
+    """The CPU oracle on the same sweep.  Set-up (drawing the inputs, packing
+    with the oracle's own packer, widening to fp64) is outside any timing; a
+    step runs the oracle's dequantize-then-matmul for every width on the first
+    `cols` output columns."""
+
+    def __init__(self):
+        import oracle
+        import synthetic
+        oracle.build()
+        self.oracle = oracle
+        self.probs = [synthetic.decode_sweep(b) for b in BITS]
+        self.packed = [oracle.pack(p.codes, p.bits)[0] for p in self.probs]
+        self.x = [p.x_f64() for p in self.probs]
+        self.s = [p.scales.astype(np.float64) for p in self.probs]
+
+    def bytes(self, cols: int) -> int:
+        return sum(cols * p.K * p.bits // 8 + cols * (p.K // p.group) * 2 + p.M * p.K * 2
+                   + p.M * cols * 2 for p in self.probs)
+
+    def step(self, cols: int):
+        for p, pk, x, s in zip(self.probs, self.packed, self.x, self.s):
+            self.oracle.qmm(x, pk[:cols], p.bits, p.group, s[:cols], None, p.zero_const, p.K)
+
+    def threads(self, cols: int) -> int:
+        return self.oracle.threads_used(0, cols)
+
+
+def oracle_baseline(sweep: OracleSweep, min_seconds: float = 3.0):
+    """Whole sweep (all widths, all columns), repeated for at least min_seconds."""
+    cols = sweep.probs[0].N
+    sweep.step(cols)  # warm
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        sweep.step(cols)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    gbs = sweep.bytes(cols) * reps / dt / 1e9
+    sample = (f"the full sweep (8 widths x 4096 columns, {sweep.bytes(cols) / 1e6:.1f} MB of "
+              f"algorithmic bytes) repeated {reps} times ({dt:.1f} s)")
+    return gbs, sweep.threads(cols), sample
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    sweep = OracleSweep()
+    full = sweep.probs[0].N
+    # size each step so that W + K steps take about a minute
+    t0 = time.perf_counter()
+    sweep.step(full)
+    t_full = time.perf_counter() - t0
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    cols = int(min(full, max(16, full * budget / max(t_full, 1e-6))))
+    cols = max(16, (cols // 16) * 16)
+    for _ in range(args.warmup):
+        sweep.step(cols)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        sweep.step(cols)
+    total = time.perf_counter() - t0
+    value = sweep.bytes(cols) * args.steps / total / 1e9
+    threads = sweep.threads(cols)
+    sample = (f"every width b=1..8, first {cols} of {full} output columns, full K "
+              f"(oracle fp64, {threads} threads)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---- GPU leg -------------------------------------------------------------------------------
+def _libcuda():
+    return ctypes.CDLL("libcuda.so.1")
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import bit_weight_quantized_gb300 as q
+    import synthetic
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    q.load()
+    stream = torch.cuda.Stream(device=dev)
+    probs = [synthetic.decode_sweep(b) for b in BITS]
+    step_bytes = sum(p.algorithmic_bytes() for p in probs)
+    per_copy = sum(p.N * p.K * p.bits // 8 + p.scales.size * 2 for p in probs)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    copies = max(args.copies, -(-2 * l2 // per_copy) + 1)
+
+    # device inputs: codes packed by qmm_pack on the GPU, replicated per copy
+    with torch.cuda.stream(stream):
+        xs, ys, sets = [], [], []
+        for p in probs:
+            xs.append(torch.from_numpy(p.x.view(np.int16)).view(torch.float16).to(dev))
+            ys.append(torch.empty((p.M, p.N), dtype=torch.float16, device=dev))
+        base = []
+        for p in probs:
+            packed = q.qmm_pack(torch.from_numpy(p.codes).to(dev), p.bits)
+            sc = torch.from_numpy(p.scales.view(np.int16)).view(torch.float16).to(dev)
+            base.append((packed, sc))
+        for c in range(copies):
+            sets.append([(pk.clone(), sc.clone()) for pk, sc in base])
+        stream.synchronize()
+
+    def step(c, marks=None):
+        for i, p in enumerate(probs):
+            pk, sc = sets[c][i]
+            if marks is not None:
+                marks(2 * i)
+            q.qmm_gemv(xs[i], pk, p.bits, p.group, sc, None, p.zero_const, out=ys[i])
+            if marks is not None:
+                marks(2 * i + 1)
+
+    # eager warm-up (also caches device facts and kernel attributes before capture)
+    with torch.cuda.stream(stream):
+        for c in range(copies):
+            step(c)
+    stream.synchronize()
+    assert q.qmm_device_status(stream) == 0
+
+    # graph A: all copies, no events (the headline timing)
+    gA = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gA, stream=stream):
+        for c in range(copies):
+            step(c)
+    # graph B: same launches with timing events around each kernel
+    cu = _libcuda()
+    cu.cuEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+    nev = 2 * len(probs)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(copies)]
+    for row in events:          # torch creates the CUDA event at its first record
+        for ev in row:
+            ev.record(stream)
+    stream.synchronize()
+    gB = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gB, stream=stream):
+        cs = torch.cuda.current_stream()
+        for c in range(copies):
+            def mark(j, c=c):
+                r = cu.cuEventRecordWithFlags(ctypes.c_void_p(events[c][j].cuda_event),
+                                              ctypes.c_void_p(cs.cuda_stream), 1)
+                if r != 0:
+                    raise RuntimeError(f"cuEventRecordWithFlags failed ({r})")
+            step(c, mark)
+
+    reps = max(1, args.steps // copies)
+    steps = reps * copies
+    warm_reps = max(1, -(-args.warmup // copies))
+    for _ in range(warm_reps):
+        gA.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            gA.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    ms_max = max_over_ranks(world, ms)
+    total_bytes = sum_over_ranks(world, step_bytes * steps)
+    value = total_bytes / (ms_max * 1e-3) / 1e9
+
+    # per-kernel durations (graph B), several replays; the events were recorded
+    # by graph nodes, so they are read through the driver API
+    cu.cuEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p,
+                                      ctypes.c_void_p]
+    kdur = np.zeros(len(probs))
+    nrep_b = max(4, min(64, reps))
+    how = "timing events between the launches inside the replayed graph"
+    try:
+        for _ in range(nrep_b):
+            gB.replay()
+            stream.synchronize()
+            for c in range(copies):
+                for i in range(len(probs)):
+                    f = ctypes.c_float()
+                    r = cu.cuEventElapsedTime(ctypes.byref(f),
+                                              ctypes.c_void_p(events[c][2 * i].cuda_event),
+                                              ctypes.c_void_p(events[c][2 * i + 1].cuda_event))
+                    if r != 0:
+                        raise RuntimeError(f"cuEventElapsedTime failed ({r})")
+                    kdur[i] += f.value
+        kdur /= nrep_b * copies          # ms per launch, per width
+    except RuntimeError as exc:
+        # fall back: a graph of 16 back-to-back launches per width, timed as a whole
+        how = f"per-width graphs of 16 launches timed as a whole ({exc})"
+        kdur[:] = 0
+        for i, p in enumerate(probs):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for r in range(16):
+                    pk, sc = sets[r % copies][i]
+                    q.qmm_gemv(xs[i], pk, p.bits, p.group, sc, None, p.zero_const, out=ys[i])
+            g.replay()
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                for _ in range(8):
+                    g.replay()
+                b_.record(stream)
+            stream.synchronize()
+            kdur[i] = a.elapsed_time(b_) / (8 * 16)
+    per_width = {}
+    for i, p in enumerate(probs):
+        gb = p.algorithmic_bytes() / (kdur[i] * 1e-3) / 1e9
+        per_width[str(p.bits)] = {"us": round(kdur[i] * 1e3, 3), "GBps": round(gb, 1)}
+    peak, peak_kind = measured_peaks()
+    achieved = step_bytes / (kdur.sum() * 1e-3) / 1e9
+    for k in per_width:
+        per_width[k]["frac"] = round(per_width[k]["GBps"] / peak, 4)
+    traffic = profile_traffic()
+
+    # e2e through the public API with host buffers: per width, copy the step's
+    # activations in from pinned memory, run, read the output back
+    xh = [torch.from_numpy(p.x.view(np.int16)).view(torch.float16).pin_memory() for p in probs]
+    yh = [torch.empty((p.M, p.N), dtype=torch.float16).pin_memory() for p in probs]
+    e2e_steps = max(20, min(500, args.steps // 20))
+    xd = [torch.empty_like(x, device=dev) for x in xh]
+    for it in range(e2e_steps + 5):
+        if it == 5:
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            c = it % copies
+            for i, p in enumerate(probs):
+                xd[i].copy_(xh[i], non_blocking=True)
+                pk, sc = sets[c][i]
+                q.qmm_gemv(xd[i], pk, p.bits, p.group, sc, None, p.zero_const, out=ys[i])
+                yh[i].copy_(ys[i], non_blocking=True)
+        stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e_s = max_over_ranks(world, e2e_s)
+    e2e_value = sum_over_ranks(world, step_bytes * e2e_steps) / e2e_s / 1e9
+    h2d = sum(x.numel() * 2 for x in xh)
+    d2h = sum(y.numel() * 2 for y in yh)
+
+    assert q.qmm_device_status(stream) == 0
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, threads, sample = oracle_baseline(OracleSweep())
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": steps, "warmup": warm_reps * copies, "ms_per_step": round(ms_max / steps, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD,
+                       "step": "8 qmm_gemv calls (b=1..8), replayed from a CUDA graph",
+                       "l2": f"inputs larger than L2: {copies} rotating copies of the step's "
+                             f"weights ({copies * per_copy / 1e6:.0f} MB > 2 x {l2 / 1e6:.0f} MB L2)",
+                       "step_bytes": step_bytes, "parallelism": f"{world} independent replicas"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "peak_kind": peak_kind,
+                         "traffic": traffic, "kernel": "qmm::gemv_kernel (all widths)",
+                         "algorithmic_bytes_per_launch": round(step_bytes / len(probs)),
+                         "frac_of_8TBs": round(achieved / 8000.0, 4),
+                         "duration_source": how},
+            "per_width": per_width,
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h,
+                    "how": "qmm_gemv through the Python binding, activations copied in from "
+                           "pinned host memory and outputs read back every call"},
+            "gpu_launches": steps * len(probs),
+            "clocks": clk,
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--copies", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -132,7 +132,8 @@ def _qmm(name, x, packed, bits, group, scales, zeros, zero_const, out, out_dtype
         _dev(zeros, "zeros", torch.uint8, (N, K // group))
     if x.dtype not in _DT:
         raise ValueError("x must be float16 or bfloat16")
-    out_dtype = out_dtype or x.dtype
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else x.dtype
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=x.device)
     _dev(out, "out", out_dtype, (M, N))

@@ -1,4 +1,5 @@
-// gemv.h -- host interface of the skinny (M <= 16) kernel.
+// gemv.h -- host interface of the skinny kernel (decode / small batches) and
+// of the shared host helpers.
 #pragma once
 
 #include <cstdint>
@@ -10,7 +11,10 @@
 namespace qmm {
 
 struct GemvParams {
-    const uint16_t *x;        // fp16 [M][K]
+    const uint16_t *x;        // fp16 [M][K]                      (qmm_gemv)
+    const int8_t *xq;         // int8 [M][K]                      (qmm_w4a8)
+    const uint16_t *sa;       // fp16 [M] per-token scales        (qmm_w4a8)
+    int32_t *acc_out;         // int32 [M][N][K/G] or nullptr     (qmm_w4a8)
     const uint8_t *packed;    // [N][K*b/8]
     const uint16_t *scales;   // fp16 [N][K/G]
     const uint8_t *zeros;     // uint8 [N][K/G] or nullptr
@@ -18,30 +22,46 @@ struct GemvParams {
     int *status;              // device status word
     long long row_bytes;      // K*b/8
     int M, N, K, group, ng, zero_const, y_bf16, use_tma;
-    // filled by gemv_plan
+    // filled by skinny_plan
     int nchunks;              // ceil(K/128)
     int stages_per_block;     // TMA stages per row block
+    int phase_chunks;         // chunks whose activations are staged at once
+    int nphases;
     int rows_base, rows_rem;  // CTA c owns rows_base + (c < rows_rem) rows
     int rb, rbp;              // rows per block, rounded up to 16
     int ring, stage_bytes, tile_bytes;
     int off_bar, off_x, off_xs, off_sz, off_red, sz_pitch;
 };
 
-// Chooses grid, row blocking and the shared-memory layout.  QMM_ERR_UNSUPPORTED
-// if the activations do not fit in shared memory next to a 4-stage ring.
-qmm_status gemv_plan(GemvParams &p, int bits, int num_sms, int smem_max, int *grid, int *smem);
+// Chooses grid, row blocking, K phases and the shared-memory layout.
+// QMM_ERR_UNSUPPORTED if no layout fits.
+qmm_status skinny_plan(GemvParams &p, int bits, int num_sms, int smem_max, int *grid, int *smem);
 
-// Launches the kernel for `bits` (tensor map used only when p.use_tma).
-cudaError_t gemv_launch(const CUtensorMap &tmap, const GemvParams &p, int bits, int grid,
-                        int smem, cudaStream_t stream);
+// 128-code chunks per TMA stage for width b (the stage box is 16*b*cs bytes wide).
+int skinny_stage_chunks(int bits);
 
-// Chunks of 128 codes per TMA stage for width b (the stage box is
-// 16*b*cs bytes wide).
-int gemv_stage_chunks(int bits);
+// Per-width launchers (one translation unit each).
+cudaError_t gemv_launch_w1(const CUtensorMap &, const GemvParams &, int, int, cudaStream_t);
+cudaError_t gemv_launch_w2(const CUtensorMap &, const GemvParams &, int, int, cudaStream_t);
+cudaError_t gemv_launch_w3(const CUtensorMap &, const GemvParams &, int, int, cudaStream_t);
+cudaError_t gemv_launch_w4(const CUtensorMap &, const GemvParams &, int, int, cudaStream_t);
+cudaError_t gemv_launch_w5(const CUtensorMap &, const GemvParams &, int, int, cudaStream_t);
+cudaError_t gemv_launch_w6(const CUtensorMap &, const GemvParams &, int, int, cudaStream_t);
+cudaError_t gemv_launch_w7(const CUtensorMap &, const GemvParams &, int, int, cudaStream_t);
+cudaError_t gemv_launch_w8(const CUtensorMap &, const GemvParams &, int, int, cudaStream_t);
+cudaError_t w4a8_launch(const CUtensorMap &, const GemvParams &, int, int, cudaStream_t);
 
 cudaError_t launch_pack(const uint8_t *codes, uint8_t *packed, int N, int K, int bits,
                         int32_t *bad_count, cudaStream_t stream, int num_sms);
 cudaError_t launch_unpack(const uint8_t *packed, uint8_t *codes, int N, int K, int bits,
                           cudaStream_t stream, int num_sms);
+
+// Tensor maps (api.cu).  A 2-D map over a byte matrix [rows][row_bytes] with a
+// box_cols x box_rows box; and over a 16-bit matrix [rows][cols] with the
+// 128-byte swizzle.
+bool encode_byte_tmap(CUtensorMap *map, const void *base, long long row_bytes, long long rows,
+                      int box_cols, int box_rows, bool swizzle128);
+bool encode_u16_tmap(CUtensorMap *map, const void *base, long long cols, long long rows,
+                     int box_cols, int box_rows);
 
 }  // namespace qmm

@@ -1,0 +1,590 @@
+// skinny.cuh -- the decode / skinny quantized matmul kernel (sm_103a).
+//
+// Computes, for a weight matrix stored as per-column LSB-first b-bit streams,
+//
+//   y[m][n] = sum_g s[n][g] * ( sum_{k in g} q[n][k] x[m][k]  -  z[n][g] X[m][g] ),
+//   X[m][g] = sum_{k in g} x[m][k],
+//
+// which is sum_k x[m][k] * s (q - z) -- BitLLM Eq. (5) with the zero-point term
+// factored out of each group so that the tensor cores only see exact integer
+// codes.  The same kernel runs the integer-native W4A8 variant (BitLLM
+// sec. 4.3-4.4): signed int4 weights w = (c xor 8) - 8, int8 activations, an
+// exact per-group integer accumulator acc = sum u x - 8 X (u = c xor 8), and a
+// deferred epilogue y = sa[m] * sum_g ws[n][g] * acc.  Products of 4-bit and
+// 8-bit integers and their group sums (|sum| <= 128*15*127 < 2^24) are exact in
+// fp16 x fp16 -> fp32 tensor-core arithmetic, and GB300's fp16 tensor path is
+// several times faster than its int8 paths, so the integer pipeline runs there.
+//
+// Work split.  CTA c owns a contiguous range of output columns (rows of the
+// packed matrix) and the whole K range; rows are processed in blocks of at most
+// 16*MAXT.  Warp 0 streams the block's bitstream through a ring of shared-memory
+// stages with one 2-D TMA tile load per stage (rows x CS 128-code chunks).  The
+// eight consumer warps split K: warp w takes every 8th chunk; their partial sums
+// meet in shared memory and are added in a fixed order (deterministic).
+// Activations are staged once per CTA (or once per K phase when M x K does not
+// fit) in "slot" order -- the order in which codes come out of the registers.
+//
+// Inside a chunk each 16-row tile takes one mma.sync.m16n8k16 per 16 codes and
+// 8 tokens.  The four threads of an MMA quad own runs of R = G/4 consecutive
+// codes of one group, so every MMA stays inside a group and the group's scale
+// is applied in fp32.  Codes become fp16 in registers with no shared-memory
+// round trip: a LOP3 keeps one code in each half of a 32-bit window and sets the
+// half's exponent so that it reads 2^E + q exactly; an exact HSUB2 removes 2^E.
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+#include "gemv.h"
+#include "unpack_plans.h"
+
+namespace qmm {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+
+// 128-code chunks per TMA stage: odd, so that the dense smem row pitch 16*b*CS
+// makes the quad-strided run reads bank-conflict free, and 16*b*CS <= 256 (the
+// TMA box limit).  b = 8 uses one 128-byte chunk with the 128-byte swizzle.
+__host__ __device__ constexpr int width_cs(int b)
+{
+    return b == 1 ? 15 : b == 2 ? 7 : b == 3 ? 5 : (b == 4 || b == 5) ? 3 : 1;
+}
+
+template <int B> struct Width {
+    static constexpr int CS = width_cs(B);
+    static constexpr int ROW_BYTES = 16 * B * CS;   // bytes of one row in a stage
+    static constexpr bool SWIZZLE = (B == 8);
+};
+
+// Byte offset of (row, byte) inside a stage, with the 128-byte swizzle (16-byte
+// chunk index XOR row mod 8) when the stage was loaded with it.
+template <int B>
+__device__ __forceinline__ uint32_t stage_off(int row, int byte)
+{
+    const uint32_t logical = static_cast<uint32_t>(row * Width<B>::ROW_BYTES + byte);
+    if constexpr (Width<B>::SWIZZLE)
+        return logical ^ (((logical >> 7) & 7u) << 4);
+    else
+        return logical;
+}
+
+// The run of R codes starting at code `code0` of a stage row, as NW words
+// shifted so that the run starts at bit 0 of w[0].
+template <int B, int R>
+__device__ __forceinline__ void load_run(const uint8_t *stage, int row, int code0,
+                                         uint32_t (&w)[(R * B + 31) / 32])
+{
+    constexpr int NW = (R * B + 31) / 32;
+    const int bit0 = code0 * B;
+    if constexpr (B == 8) {
+        if constexpr (R >= 16) {
+#pragma unroll
+            for (int i = 0; i < NW; i += 4) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(stage + stage_off<B>(row, code0 + 4 * i));
+                w[i] = v.x; w[i + 1] = v.y; w[i + 2] = v.z; w[i + 3] = v.w;
+            }
+        } else {
+            const uint2 v = *reinterpret_cast<const uint2 *>(stage + stage_off<B>(row, code0));
+            w[0] = v.x; w[1] = v.y;
+        }
+    } else if constexpr ((R * B) % 32 == 0 && B == 4 && NW == 4) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(stage + stage_off<B>(row, bit0 / 8));
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else if constexpr ((R * B) % 32 == 0) {
+        const int wi = bit0 / 32;
+        if constexpr (B % 2 == 0 && NW % 2 == 0) {
+#pragma unroll
+            for (int i = 0; i < NW; i += 2) {
+                const uint2 v = *reinterpret_cast<const uint2 *>(stage + stage_off<B>(row, 4 * (wi + i)));
+                w[i] = v.x; w[i + 1] = v.y;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < NW; ++i)
+                w[i] = *reinterpret_cast<const uint32_t *>(stage + stage_off<B>(row, 4 * (wi + i)));
+        }
+    } else {
+        // the run starts inside a word: read NW+1 words and funnel-shift
+        const int wi = bit0 / 32;
+        const int sh = bit0 & 31;
+        uint32_t src[NW + 1];
+#pragma unroll
+        for (int i = 0; i <= NW; ++i)
+            src[i] = *reinterpret_cast<const uint32_t *>(stage + stage_off<B>(row, 4 * (wi + i)));
+#pragma unroll
+        for (int i = 0; i < NW; ++i)
+            w[i] = __funnelshift_r(src[i], src[i + 1], sh);
+    }
+}
+
+template <int B, int R, int NW>
+__device__ __forceinline__ uint32_t plan_window(const uint32_t (&w)[NW], int v)
+{
+    using P = UnpackPlan<B, R>;
+    if (P::kind(v) == 1)
+        return prmt(w[P::w0(v)], w[P::w1(v)], P::sel(v));
+    const int o = P::off(v);
+    if (o < 0)
+        return w[0] << (-o);
+    const int i = o >> 5, s = o & 31;
+    if (s == 0)
+        return w[i];
+    if (i + 1 < NW)
+        return __funnelshift_r(w[i], w[i + 1], s);
+    return w[i] >> s;
+}
+
+__host__ __device__ constexpr uint32_t pow2_half_bits(int e)
+{
+    return static_cast<uint32_t>(e + 15) << 10;  // fp16 bits of 2^e
+}
+
+__device__ __forceinline__ uint32_t lop3_and_xor(uint32_t a, uint32_t mask, uint32_t bits)
+{
+    // (a & mask) ^ bits
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(mask), "r"(bits));
+    return d;
+}
+
+// a[i] = fp16 pair (q_lo, q_hi) of plan pair i, exact small integers.  With
+// FLIP8 each 4-bit field is XORed with 8 first (signed int4 -> c xor 8).
+template <int B, int R, bool FLIP8>
+__device__ __forceinline__ void extract_run(const uint32_t (&w)[(R * B + 31) / 32],
+                                            uint32_t (&a)[R / 2])
+{
+    constexpr int NW = (R * B + 31) / 32;
+    if constexpr (B == 8) {
+#pragma unroll
+        for (int i = 0; i < R / 2; ++i) {
+            const uint32_t v = prmt(w[i >> 1], 0x64646464u, (i & 1) ? 0x4342u : 0x4140u);
+            a[i] = hsub2(v, 0x64006400u);
+        }
+    } else {
+        using P = UnpackPlan<B, R>;
+        uint32_t win[P::kWindows];
+#pragma unroll
+        for (int v = 0; v < P::kWindows; ++v)
+            win[v] = plan_window<B, R, NW>(w, v);
+#pragma unroll
+        for (int i = 0; i < R / 2; ++i) {
+            uint32_t v;
+            if constexpr (FLIP8)
+                v = lop3_and_xor(win[P::win(i)], P::mask(i),
+                                 P::magic(i) | (P::mask(i) & 0x88888888u));
+            else
+                v = lop3_and_or(win[P::win(i)], P::mask(i), P::magic(i));
+            a[i] = hsub2(v, pow2_half_bits(P::elo(i)) | (pow2_half_bits(P::ehi(i)) << 16));
+        }
+    }
+}
+
+// Code of the run that feeds slot s = 4*j + e of the activation fragments.
+template <int B, int R>
+__device__ __forceinline__ constexpr int code_of_slot(int s)
+{
+    if constexpr (B == 8) {
+        return s;  // pairs are (2i, 2i+1): slot order is code order
+    } else {
+        using P = UnpackPlan<B, R>;
+        const int i = 2 * (s >> 2) + ((s >> 1) & 1);
+        return (s & 1) ? P::hi(i) : P::lo(i);
+    }
+}
+
+__device__ __forceinline__ uint16_t s8_to_f16_bits(int v)
+{
+    uint16_t h;
+    asm("cvt.rn.f16.s32 %0, %1;" : "=h"(h) : "r"(v));
+    return h;
+}
+
+// Stages the activations of chunks [ch0, ch0 + nch) in slot order, and the
+// per-group sums X.  MODE 0 reads fp16 x, MODE 1 int8 xq (converted exactly).
+template <int B, int R, int MODE, int MP>
+__device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t *xp, float *xs,
+                                                  int ch0, int nch, int ct)
+{
+    constexpr int G = 4 * R;
+    constexpr int NGC = 128 / G;
+    const int M = p.M;
+    const int ngp = nch * NGC;
+    for (int idx = ct; idx < M * ngp; idx += 32 * kConsumerWarps) {
+        const int m = idx / ngp;
+        const int lg = idx - m * ngp;
+        const int grp = ch0 * NGC + lg;
+        const int lc = lg / NGC;
+        const int gi = lg - lc * NGC;
+        float sum = 0.f;
+#pragma unroll 1
+        for (int tt = 0; tt < 4; ++tt) {
+            const int k0 = grp * G + tt * R;
+            uint16_t v[R];
+            if constexpr (MODE == 0) {
+#pragma unroll
+                for (int c = 0; c < R; c += 8) {
+                    uint4 q = make_uint4(0, 0, 0, 0);
+                    if (k0 + c < p.K)
+                        q = *reinterpret_cast<const uint4 *>(p.x + static_cast<long long>(m) * p.K + k0 + c);
+                    v[c + 0] = q.x & 0xFFFF; v[c + 1] = q.x >> 16;
+                    v[c + 2] = q.y & 0xFFFF; v[c + 3] = q.y >> 16;
+                    v[c + 4] = q.z & 0xFFFF; v[c + 5] = q.z >> 16;
+                    v[c + 6] = q.w & 0xFFFF; v[c + 7] = q.w >> 16;
+                }
+#pragma unroll
+                for (int c = 0; c < R; ++c)
+                    sum += f16_bits_to_f32(v[c]);
+            } else {
+                int isum = 0;
+#pragma unroll
+                for (int c = 0; c < R; c += 8) {
+                    uint2 q = make_uint2(0, 0);
+                    if (k0 + c < p.K)
+                        q = *reinterpret_cast<const uint2 *>(p.xq + static_cast<long long>(m) * p.K + k0 + c);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const uint32_t word = e < 4 ? q.x : q.y;
+                        const int val = static_cast<int>(static_cast<int8_t>((word >> (8 * (e & 3))) & 0xFF));
+                        v[c + e] = s8_to_f16_bits(val);
+                        isum += val;
+                    }
+                }
+                sum += static_cast<float>(isum);  // exact: |sum| <= 128 * 127
+            }
+#pragma unroll
+            for (int j = 0; j < R / 4; ++j) {
+                uint2 o;
+                o.x = v[code_of_slot<B, R>(4 * j + 0)] | (static_cast<uint32_t>(v[code_of_slot<B, R>(4 * j + 1)]) << 16);
+                o.y = v[code_of_slot<B, R>(4 * j + 2)] | (static_cast<uint32_t>(v[code_of_slot<B, R>(4 * j + 3)]) << 16);
+                const int jj = gi * (R / 4) + j;
+                *reinterpret_cast<uint2 *>(xp + ((static_cast<long long>(lc) * 8 + jj) * M + m) * 16 + tt * 4) = o;
+            }
+        }
+        xs[lg * MP + m] = sum;
+    }
+    for (int idx = ct; idx < (MP - M) * ngp; idx += 32 * kConsumerWarps) {
+        const int mm = M + idx / ngp;
+        const int lg = idx % ngp;
+        xs[lg * MP + mm] = 0.f;
+    }
+}
+
+template <int B, int NT, int R, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+skinny_kernel(const __grid_constant__ CUtensorMap tmap, const GemvParams p)
+{
+    constexpr int MP = 8 * NT;                 // padded token count of the D fragments
+    constexpr int NGC = 128 / (4 * R);         // groups per 128-code chunk
+    constexpr int MAXT = NT <= 2 ? 8 : 16 / NT;   // 16-row tiles per block
+    constexpr int CS = Width<B>::CS;
+    constexpr bool FLIP8 = (MODE == 1);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *ring = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
+    uint64_t *empty = full + p.ring;
+    uint16_t *xp = reinterpret_cast<uint16_t *>(smem + p.off_x);   // [chunk][8][M][4][4]
+    float *xs = reinterpret_cast<float *>(smem + p.off_xs);        // [group][MP]
+    float2 *sz = reinterpret_cast<float2 *>(smem + p.off_sz);      // [row][sz_pitch] (s, z*s)
+    float *red = reinterpret_cast<float *>(smem + p.off_red);      // [warp][rbp][MP]
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const int r0 = cta * p.rows_base + min(cta, p.rows_rem);
+    const int nrows = p.rows_base + (cta < p.rows_rem ? 1 : 0);
+    const int nblocks = (nrows + p.rb - 1) / p.rb;
+    const int total_stages = nblocks * p.stages_per_block;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.ring; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ================= producer =================
+        bool ok = true;
+        int issued = 0;
+        if (p.use_tma && lane == 0)
+            prefetch_tmap(&tmap);
+        for (int it = 0; it < total_stages && ok; ++it) {
+            const int slot = it % p.ring;
+            const int round = it / p.ring;
+            if (round > 0)
+                ok = mbar_wait(&empty[slot], (round - 1) & 1, p.status);
+            if (!ok)
+                break;
+            const int blk = it / p.stages_per_block;
+            const int s = it - blk * p.stages_per_block;
+            const int row0 = r0 + blk * p.rb;
+            uint8_t *dst = ring + static_cast<size_t>(slot) * p.stage_bytes;
+            if (p.use_tma) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[slot], p.tile_bytes);
+                    tma_load_2d(dst, &tmap, &full[slot], s * Width<B>::ROW_BYTES, row0);
+                }
+            } else {
+                // plain 4-byte copies (row pitch of the packed matrix not 16-byte aligned)
+                const int words_per_row = Width<B>::ROW_BYTES / 4;
+                for (int e = lane; e < p.rb * words_per_row; e += 32) {
+                    const int r = e / words_per_row;
+                    const int wo = e - r * words_per_row;
+                    const long long byte = static_cast<long long>(s) * Width<B>::ROW_BYTES + 4 * wo;
+                    uint32_t v = 0;
+                    if (row0 + r < p.N && byte < p.row_bytes)
+                        v = *reinterpret_cast<const uint32_t *>(p.packed + static_cast<long long>(row0 + r) * p.row_bytes + byte);
+                    *reinterpret_cast<uint32_t *>(dst + stage_off<B>(r, 4 * wo)) = v;
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&full[slot]);
+            }
+            ++issued;
+        }
+        // drain: no copy into this CTA's shared memory may still be in flight
+        if (lane == 0) {
+            const int first = issued > p.ring ? issued - p.ring : 0;
+            for (int it = first; it < issued; ++it)
+                if (!mbar_wait(&full[it % p.ring], (it / p.ring) & 1, p.status))
+                    break;
+        }
+        return;
+    }
+
+    // ================= consumers =================
+    const int cw = warp - 1;              // consumer warp 0..7
+    const int ct = threadIdx.x - 32;      // consumer thread 0..255
+    const int g = lane >> 2, t = lane & 3;
+    const int M = p.M;
+    const int ng = p.ng;
+    constexpr int kCT = 32 * kConsumerWarps;
+
+    if (p.nphases == 1)
+        stage_activations<B, R, MODE, MP>(p, xp, xs, 0, p.nchunks, ct);
+
+    bool ok = true;
+    int it = 0;
+    for (int blk = 0; blk < nblocks; ++blk) {
+        const int row0 = r0 + blk * p.rb;
+        const int rows_valid = min(p.rb, r0 + nrows - row0);
+        const int T = (rows_valid + 15) / 16;
+
+        named_sync(1, kCT);   // the previous block's epilogue is done with sz / red
+        for (int idx = ct; idx < rows_valid * ng; idx += kCT) {
+            const int r = idx / ng;
+            const int grp = idx - r * ng;
+            const long long off = static_cast<long long>(row0 + r) * ng + grp;
+            const float s = f16_bits_to_f32(p.scales[off]);
+            const float z = p.zeros ? static_cast<float>(p.zeros[off]) : static_cast<float>(p.zero_const);
+            sz[r * p.sz_pitch + grp] = make_float2(s, z * s);
+        }
+        named_sync(1, kCT);
+
+        float tot[MAXT][NT][4];
+#pragma unroll
+        for (int mt = 0; mt < MAXT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    tot[mt][nt][e] = 0.f;
+
+        int cur_phase = p.nphases == 1 ? 0 : -1;
+        for (int s = 0; s < p.stages_per_block; ++s, ++it) {
+            const int phase = (s * CS) / p.phase_chunks;
+            if (phase != cur_phase) {
+                named_sync(1, kCT);   // everyone is done with the previous phase
+                const int ch0 = phase * p.phase_chunks;
+                stage_activations<B, R, MODE, MP>(p, xp, xs, ch0, min(p.phase_chunks, p.nchunks - ch0), ct);
+                named_sync(1, kCT);
+                cur_phase = phase;
+            }
+            const int slot = it % p.ring;
+            if (ok)
+                ok = mbar_wait(&full[slot], (it / p.ring) & 1, p.status);
+            if (ok) {
+                const uint8_t *stage = ring + static_cast<size_t>(slot) * p.stage_bytes;
+#pragma unroll 1
+                for (int ci = 0; ci < CS; ++ci) {
+                    const int cg = s * CS + ci;
+                    if (cg >= p.nchunks)
+                        break;
+                    if ((cg & (kConsumerWarps - 1)) != cw)
+                        continue;
+                    const int lc = cg - phase * p.phase_chunks;   // chunk within the phase
+#pragma unroll 1
+                    for (int gi = 0; gi < NGC; ++gi) {
+                        const int grp = cg * NGC + gi;
+                        if (grp >= ng)
+                            break;
+                        const int lg = lc * NGC + gi;
+                        const uint16_t *xb = xp + (static_cast<long long>(lc) * 8 + gi * (R / 4)) * M * 16 + t * 4;
+                        // activation fragments for the R/4 MMAs (hoisted for small NT)
+                        uint32_t bf[NT <= 2 ? R / 4 : 1][NT <= 2 ? NT : 1][2];
+                        if constexpr (NT <= 2) {
+#pragma unroll
+                            for (int j = 0; j < R / 4; ++j)
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt) {
+                                    const int m = g + 8 * nt;
+                                    uint2 v = make_uint2(0, 0);
+                                    if (m < M)
+                                        v = *reinterpret_cast<const uint2 *>(xb + (j * M + m) * 16);
+                                    bf[j][nt][0] = v.x;
+                                    bf[j][nt][1] = v.y;
+                                }
+                        }
+                        const int code0 = ci * 128 + gi * 4 * R + t * R;   // within the stage row
+#pragma unroll
+                        for (int mt = 0; mt < MAXT; ++mt) {
+                            if (mt < T) {
+                                const int lr0 = mt * 16 + g;
+                                uint32_t w0[(R * B + 31) / 32], w1[(R * B + 31) / 32];
+                                load_run<B, R>(stage, lr0, code0, w0);
+                                load_run<B, R>(stage, lr0 + 8, code0, w1);
+                                uint32_t a0[R / 2], a1[R / 2];
+                                extract_run<B, R, FLIP8>(w0, a0);
+                                extract_run<B, R, FLIP8>(w1, a1);
+                                const float2 sz0 = sz[lr0 * p.sz_pitch + grp];
+                                const float2 sz1 = sz[(lr0 + 8) * p.sz_pitch + grp];
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt) {
+                                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                                    for (int j = 0; j < R / 4; ++j) {
+                                        uint32_t b0, b1;
+                                        if constexpr (NT <= 2) {
+                                            b0 = bf[j][nt][0];
+                                            b1 = bf[j][nt][1];
+                                        } else {
+                                            const int m = g + 8 * nt;
+                                            uint2 v = make_uint2(0, 0);
+                                            if (m < M)
+                                                v = *reinterpret_cast<const uint2 *>(xb + (j * M + m) * 16);
+                                            b0 = v.x;
+                                            b1 = v.y;
+                                        }
+                                        mma_f16_16816(d, a0[2 * j], a1[2 * j], a0[2 * j + 1], a1[2 * j + 1], b0, b1);
+                                    }
+                                    const float2 xv = *reinterpret_cast<const float2 *>(xs + lg * MP + 8 * nt + 2 * t);
+                                    if constexpr (MODE == 0) {
+                                        tot[mt][nt][0] = fmaf(-sz0.y, xv.x, fmaf(sz0.x, d[0], tot[mt][nt][0]));
+                                        tot[mt][nt][1] = fmaf(-sz0.y, xv.y, fmaf(sz0.x, d[1], tot[mt][nt][1]));
+                                        tot[mt][nt][2] = fmaf(-sz1.y, xv.x, fmaf(sz1.x, d[2], tot[mt][nt][2]));
+                                        tot[mt][nt][3] = fmaf(-sz1.y, xv.y, fmaf(sz1.x, d[3], tot[mt][nt][3]));
+                                    } else {
+                                        // exact integers: d and 8 X are below 2^24
+                                        const float acc0 = d[0] - 8.f * xv.x, acc1 = d[1] - 8.f * xv.y;
+                                        const float acc2 = d[2] - 8.f * xv.x, acc3 = d[3] - 8.f * xv.y;
+                                        tot[mt][nt][0] = fmaf(sz0.x, acc0, tot[mt][nt][0]);
+                                        tot[mt][nt][1] = fmaf(sz0.x, acc1, tot[mt][nt][1]);
+                                        tot[mt][nt][2] = fmaf(sz1.x, acc2, tot[mt][nt][2]);
+                                        tot[mt][nt][3] = fmaf(sz1.x, acc3, tot[mt][nt][3]);
+                                        if (p.acc_out) {
+                                            const int tok = 8 * nt + 2 * t;
+                                            const int n0 = row0 + lr0;
+                                            const bool v0 = lr0 < rows_valid, v1 = lr0 + 8 < rows_valid;
+                                            const long long base0 = static_cast<long long>(n0) * ng + grp;
+                                            const long long base1 = static_cast<long long>(n0 + 8) * ng + grp;
+                                            const long long tstride = static_cast<long long>(p.N) * ng;
+                                            if (v0 && tok < M) p.acc_out[tok * tstride + base0] = static_cast<int>(acc0);
+                                            if (v0 && tok + 1 < M) p.acc_out[(tok + 1) * tstride + base0] = static_cast<int>(acc1);
+                                            if (v1 && tok < M) p.acc_out[tok * tstride + base1] = static_cast<int>(acc2);
+                                            if (v1 && tok + 1 < M) p.acc_out[(tok + 1) * tstride + base1] = static_cast<int>(acc3);
+                                        }
+                                    }
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[slot]);
+        }
+
+        // ---- cross-warp reduction in a fixed order, then the store ----
+#pragma unroll
+        for (int mt = 0; mt < MAXT; ++mt) {
+            if (mt < T) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int row = mt * 16 + g;
+                    const int tok = 8 * nt + 2 * t;
+                    *reinterpret_cast<float2 *>(red + (cw * p.rbp + row) * MP + tok) =
+                        make_float2(tot[mt][nt][0], tot[mt][nt][1]);
+                    *reinterpret_cast<float2 *>(red + (cw * p.rbp + row + 8) * MP + tok) =
+                        make_float2(tot[mt][nt][2], tot[mt][nt][3]);
+                }
+            }
+        }
+        named_sync(1, kCT);
+        for (int idx = ct; idx < M * rows_valid; idx += kCT) {
+            const int tok = idx / rows_valid;
+            const int row = idx - tok * rows_valid;
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w)
+                v += red[(w * p.rbp + row) * MP + tok];
+            if constexpr (MODE == 1)
+                v *= f16_bits_to_f32(p.sa[tok]);
+            const long long o = static_cast<long long>(tok) * p.N + row0 + row;
+            if (p.y_bf16)
+                reinterpret_cast<uint16_t *>(p.y)[o] = f32_to_bf16_bits(v);
+            else
+                reinterpret_cast<uint16_t *>(p.y)[o] = f32_to_f16_bits(v);
+        }
+    }
+}
+
+// ---- host-side launch of one instantiation ----------------------------------------------
+template <int B, int NT, int R, int MODE>
+cudaError_t launch_skinny(const CUtensorMap &tmap, const GemvParams &p, int grid, int smem,
+                          cudaStream_t stream)
+{
+    auto kern = skinny_kernel<B, NT, R, MODE>;
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    if (configured[dev] < smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess)
+            return e;
+        configured[dev] = smem;
+    }
+    kern<<<grid, kThreads, smem, stream>>>(tmap, p);
+    return cudaGetLastError();
+}
+
+template <int B, int MODE>
+cudaError_t launch_skinny_width(const CUtensorMap &tmap, const GemvParams &p, int grid, int smem,
+                                cudaStream_t stream)
+{
+    const int nt = (p.M + 7) / 8;
+#define QMM_R(NTV)                                                                          \
+    switch (p.group) {                                                                      \
+    case 32: return launch_skinny<B, NTV, 8, MODE>(tmap, p, grid, smem, stream);            \
+    case 64: return launch_skinny<B, NTV, 16, MODE>(tmap, p, grid, smem, stream);           \
+    default: return launch_skinny<B, NTV, 32, MODE>(tmap, p, grid, smem, stream);           \
+    }
+    if (nt <= 1) { QMM_R(1) }
+    if (nt <= 2) { QMM_R(2) }
+    if constexpr (MODE == 1) {
+        if (nt <= 4) { QMM_R(4) }
+        QMM_R(8)
+    }
+#undef QMM_R
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace qmm

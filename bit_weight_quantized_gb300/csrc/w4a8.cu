@@ -1,13 +1,59 @@
-// w4a8.cu -- integer-native W4A8 path (placeholder until the kernel lands).
-#include "common.cuh"
+// w4a8.cu -- integer-native W4A8 (BitLLM sec. 4.3-4.4) on the skinny kernel.
+//
+// Signed int4 weights c (two's complement nibbles, the 4-bit bitstream) are
+// read as u = c xor 8 in [0, 15], so w = u - 8; int8 activations are staged as
+// exact fp16.  Per group the kernel forms D = sum u*x on fp16 tensor cores --
+// every product and partial sum is an integer below 2^24, so fp32 accumulation
+// is exact -- and acc = D - 8 * sum x, the exact int32 accumulator.  The
+// epilogue applies the per-group weight scale and per-token activation scale:
+// y = sa[m] * sum_g ws[n][g] * acc.
+#include <cstring>
+
+#include "gemv.h"
+#include "skinny.cuh"
 #include "w4a8.h"
 
 namespace qmm {
 
-qmm_status w4a8_dispatch(const int8_t *, const void *, const uint8_t *, const void *, int, void *,
-                         int32_t *, int, int, int, int *, int, int, cudaStream_t)
+cudaError_t w4a8_launch(const CUtensorMap &tmap, const GemvParams &p, int grid, int smem,
+                        cudaStream_t stream)
 {
-    return QMM_ERR_UNSUPPORTED;
+    return launch_skinny_width<4, 1>(tmap, p, grid, smem, stream);
+}
+
+qmm_status w4a8_dispatch(const int8_t *xq, const void *sa, const uint8_t *w4, const void *ws,
+                         int group, void *y, int32_t *acc_out, int M, int N, int K, int *status,
+                         int num_sms, int smem_optin, cudaStream_t stream)
+{
+    GemvParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.xq = xq;
+    p.sa = static_cast<const uint16_t *>(sa);
+    p.acc_out = acc_out;
+    p.packed = w4;
+    p.scales = static_cast<const uint16_t *>(ws);
+    p.zeros = nullptr;
+    p.zero_const = 8;
+    p.y = y;
+    p.status = status;
+    p.row_bytes = static_cast<long long>(K) / 2;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.group = group;
+    p.ng = K / group;
+    p.y_bf16 = 0;
+    int grid = 0, smem = 0;
+    qmm_status st = skinny_plan(p, 4, num_sms, smem_optin, &grid, &smem);
+    if (st != QMM_OK)
+        return st;
+    CUtensorMap tmap;
+    std::memset(&tmap, 0, sizeof(tmap));
+    p.use_tma = 0;
+    if (p.row_bytes % 16 == 0 &&
+        encode_byte_tmap(&tmap, w4, p.row_bytes, N, 16 * 4 * skinny_stage_chunks(4), p.rb, false))
+        p.use_tma = 1;
+    return w4a8_launch(tmap, p, grid, smem, stream) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
 }
 
 }  // namespace qmm

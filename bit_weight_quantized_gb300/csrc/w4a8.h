@@ -1,4 +1,4 @@
-// w4a8.h -- host interface of the integer-native W4A8 kernel.
+// w4a8.h -- host interface of the integer-native W4A8 path.
 #pragma once
 
 #include <cstdint>
