@@ -246,18 +246,22 @@ qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int
     p.zero_const = zeros ? 0 : zero_const;
     p.y_bf16 = y_dtype == QMM_BF16;
     int grid = 0, smem = 0;
-    st = gemv_plan(p, bits, f->num_sms, f->smem_optin, &grid, &smem);
+    st = skinny_plan(p, bits, f->num_sms, f->smem_optin, &grid, &smem);
     if (st != QMM_OK)
         return st;
-    CUtensorMap tmap;
-    std::memset(&tmap, 0, sizeof(tmap));
-    p.use_tma = 0;
-    if (aligned(packed, 16) && p.row_bytes % 16 == 0) {
-        const int box_cols = 16 * bits * gemv_stage_chunks(bits);
-        if (encode_byte_tmap(&tmap, packed, p.row_bytes, N, box_cols, p.rb, bits == 8))
-            p.use_tma = 1;
+    p.use_bulk = aligned(packed, 16) && p.row_bytes % 16 == 0;
+    cudaError_t e;
+    switch (bits) {
+    case 1: e = gemv_launch_w1(p, grid, smem, stream); break;
+    case 2: e = gemv_launch_w2(p, grid, smem, stream); break;
+    case 3: e = gemv_launch_w3(p, grid, smem, stream); break;
+    case 4: e = gemv_launch_w4(p, grid, smem, stream); break;
+    case 5: e = gemv_launch_w5(p, grid, smem, stream); break;
+    case 6: e = gemv_launch_w6(p, grid, smem, stream); break;
+    case 7: e = gemv_launch_w7(p, grid, smem, stream); break;
+    default: e = gemv_launch_w8(p, grid, smem, stream); break;
     }
-    return from_cuda(gemv_launch(tmap, p, bits, grid, smem, stream));
+    return from_cuda(e);
 }
 
 qmm_status qmm_gemm(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int bits,

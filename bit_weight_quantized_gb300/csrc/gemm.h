@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/qmm.h"
+#include "gemv.h"
 
 namespace qmm {
 
@@ -13,11 +14,5 @@ qmm_status gemm_dispatch(const void *x, bool x_bf16, const uint8_t *packed, int 
                          const void *scales, const uint8_t *zeros, int zero_const, void *y, int M,
                          int N, int K, int *status, int num_sms, int smem_optin,
                          cudaStream_t stream);
-
-// Tensor-map helpers defined in api.cu.
-bool encode_byte_tmap(CUtensorMap *map, const void *base, long long row_bytes, long long rows,
-                      int box_cols, int box_rows, bool swizzle128);
-bool encode_u16_tmap(CUtensorMap *map, const void *base, long long cols, long long rows,
-                     int box_cols, int box_rows);
 
 }  // namespace qmm

@@ -21,15 +21,19 @@ struct GemvParams {
     void *y;                  // [M][N]
     int *status;              // device status word
     long long row_bytes;      // K*b/8
-    int M, N, K, group, ng, zero_const, y_bf16, use_tma;
+    int M, N, K, group, ng, zero_const, y_bf16;
+    int use_bulk;             // rows 16-byte aligned: 1-D bulk copies, else plain copies
     // filled by skinny_plan
     int nchunks;              // ceil(K/128)
-    int stages_per_block;     // TMA stages per row block
+    int stages_per_block;     // K segments (pipeline stages) per row block
+    int seg_chunks;           // 128-code chunks per K segment
+    int seg_bytes;            // bytes of one row's segment (seg_chunks * 16 * b)
+    int pitch;                // shared-memory row pitch of a stage
     int phase_chunks;         // chunks whose activations are staged at once
     int nphases;
     int rows_base, rows_rem;  // CTA c owns rows_base + (c < rows_rem) rows
     int rb, rbp;              // rows per block, rounded up to 16
-    int ring, stage_bytes, tile_bytes;
+    int ring, stage_bytes;
     int off_bar, off_x, off_xs, off_sz, off_red, sz_pitch;
 };
 
@@ -37,19 +41,16 @@ struct GemvParams {
 // QMM_ERR_UNSUPPORTED if no layout fits.
 qmm_status skinny_plan(GemvParams &p, int bits, int num_sms, int smem_max, int *grid, int *smem);
 
-// 128-code chunks per TMA stage for width b (the stage box is 16*b*cs bytes wide).
-int skinny_stage_chunks(int bits);
-
 // Per-width launchers (one translation unit each).
-cudaError_t gemv_launch_w1(const CUtensorMap &, const GemvParams &, int, int, cudaStream_t);
-cudaError_t gemv_launch_w2(const CUtensorMap &, const GemvParams &, int, int, cudaStream_t);
-cudaError_t gemv_launch_w3(const CUtensorMap &, const GemvParams &, int, int, cudaStream_t);
-cudaError_t gemv_launch_w4(const CUtensorMap &, const GemvParams &, int, int, cudaStream_t);
-cudaError_t gemv_launch_w5(const CUtensorMap &, const GemvParams &, int, int, cudaStream_t);
-cudaError_t gemv_launch_w6(const CUtensorMap &, const GemvParams &, int, int, cudaStream_t);
-cudaError_t gemv_launch_w7(const CUtensorMap &, const GemvParams &, int, int, cudaStream_t);
-cudaError_t gemv_launch_w8(const CUtensorMap &, const GemvParams &, int, int, cudaStream_t);
-cudaError_t w4a8_launch(const CUtensorMap &, const GemvParams &, int, int, cudaStream_t);
+cudaError_t gemv_launch_w1(const GemvParams &, int, int, cudaStream_t);
+cudaError_t gemv_launch_w2(const GemvParams &, int, int, cudaStream_t);
+cudaError_t gemv_launch_w3(const GemvParams &, int, int, cudaStream_t);
+cudaError_t gemv_launch_w4(const GemvParams &, int, int, cudaStream_t);
+cudaError_t gemv_launch_w5(const GemvParams &, int, int, cudaStream_t);
+cudaError_t gemv_launch_w6(const GemvParams &, int, int, cudaStream_t);
+cudaError_t gemv_launch_w7(const GemvParams &, int, int, cudaStream_t);
+cudaError_t gemv_launch_w8(const GemvParams &, int, int, cudaStream_t);
+cudaError_t w4a8_launch(const GemvParams &, int, int, cudaStream_t);
 
 cudaError_t launch_pack(const uint8_t *codes, uint8_t *packed, int N, int K, int bits,
                         int32_t *bad_count, cudaStream_t stream, int num_sms);

@@ -3,10 +3,9 @@
 
 namespace qmm {
 
-cudaError_t gemv_launch_w5(const CUtensorMap &tmap, const GemvParams &p, int grid, int smem,
-                           cudaStream_t stream)
+cudaError_t gemv_launch_w5(const GemvParams &p, int grid, int smem, cudaStream_t stream)
 {
-    return launch_skinny_width<5, 0>(tmap, p, grid, smem, stream);
+    return launch_skinny_width<5, 0>(p, grid, smem, stream);
 }
 
 }  // namespace qmm

@@ -18,9 +18,12 @@
 // Work split.  CTA c owns a contiguous range of output columns (rows of the
 // packed matrix) and the whole K range; rows are processed in blocks of at most
 // 16*MAXT.  Warp 0 streams the block's bitstream through a ring of shared-memory
-// stages with one 2-D TMA tile load per stage (rows x CS 128-code chunks).  The
-// eight consumer warps split K: warp w takes every 8th chunk; their partial sums
-// meet in shared memory and are added in a fixed order (deterministic).
+// stages: a stage is one K segment (SEG 128-code chunks, about a kilobyte) of
+// every row of the block, one 1-D bulk copy (TMA) per row.  Long contiguous
+// per-row copies keep HBM efficient; the rows land at a padded pitch that makes
+// the consumers' quad-strided reads bank-conflict free.  The eight consumer
+// warps split K: warp w takes every 8th chunk; their partial sums meet in
+// shared memory and are added in a fixed order (deterministic).
 // Activations are staged once per CTA (or once per K phase when M x K does not
 // fit) in "slot" order -- the order in which codes come out of the registers.
 //
@@ -43,36 +46,16 @@ namespace qmm {
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 
-// 128-code chunks per TMA stage: odd, so that the dense smem row pitch 16*b*CS
-// makes the quad-strided run reads bank-conflict free, and 16*b*CS <= 256 (the
-// TMA box limit).  b = 8 uses one 128-byte chunk with the 128-byte swizzle.
-__host__ __device__ constexpr int width_cs(int b)
+// Byte offset of (row, byte) inside a stage: rows sit at a padded pitch.
+__device__ __forceinline__ uint32_t stage_off(int pitch, int row, int byte)
 {
-    return b == 1 ? 15 : b == 2 ? 7 : b == 3 ? 5 : (b == 4 || b == 5) ? 3 : 1;
-}
-
-template <int B> struct Width {
-    static constexpr int CS = width_cs(B);
-    static constexpr int ROW_BYTES = 16 * B * CS;   // bytes of one row in a stage
-    static constexpr bool SWIZZLE = (B == 8);
-};
-
-// Byte offset of (row, byte) inside a stage, with the 128-byte swizzle (16-byte
-// chunk index XOR row mod 8) when the stage was loaded with it.
-template <int B>
-__device__ __forceinline__ uint32_t stage_off(int row, int byte)
-{
-    const uint32_t logical = static_cast<uint32_t>(row * Width<B>::ROW_BYTES + byte);
-    if constexpr (Width<B>::SWIZZLE)
-        return logical ^ (((logical >> 7) & 7u) << 4);
-    else
-        return logical;
+    return static_cast<uint32_t>(row * pitch + byte);
 }
 
 // The run of R codes starting at code `code0` of a stage row, as NW words
 // shifted so that the run starts at bit 0 of w[0].
 template <int B, int R>
-__device__ __forceinline__ void load_run(const uint8_t *stage, int row, int code0,
+__device__ __forceinline__ void load_run(const uint8_t *stage, int pitch, int row, int code0,
                                          uint32_t (&w)[(R * B + 31) / 32])
 {
     constexpr int NW = (R * B + 31) / 32;
@@ -81,28 +64,28 @@ __device__ __forceinline__ void load_run(const uint8_t *stage, int row, int code
         if constexpr (R >= 16) {
 #pragma unroll
             for (int i = 0; i < NW; i += 4) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(stage + stage_off<B>(row, code0 + 4 * i));
+                const uint4 v = *reinterpret_cast<const uint4 *>(stage + stage_off(pitch, row, code0 + 4 * i));
                 w[i] = v.x; w[i + 1] = v.y; w[i + 2] = v.z; w[i + 3] = v.w;
             }
         } else {
-            const uint2 v = *reinterpret_cast<const uint2 *>(stage + stage_off<B>(row, code0));
+            const uint2 v = *reinterpret_cast<const uint2 *>(stage + stage_off(pitch, row, code0));
             w[0] = v.x; w[1] = v.y;
         }
     } else if constexpr ((R * B) % 32 == 0 && B == 4 && NW == 4) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(stage + stage_off<B>(row, bit0 / 8));
+        const uint4 v = *reinterpret_cast<const uint4 *>(stage + stage_off(pitch, row, bit0 / 8));
         w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
     } else if constexpr ((R * B) % 32 == 0) {
         const int wi = bit0 / 32;
         if constexpr (B % 2 == 0 && NW % 2 == 0) {
 #pragma unroll
             for (int i = 0; i < NW; i += 2) {
-                const uint2 v = *reinterpret_cast<const uint2 *>(stage + stage_off<B>(row, 4 * (wi + i)));
+                const uint2 v = *reinterpret_cast<const uint2 *>(stage + stage_off(pitch, row, 4 * (wi + i)));
                 w[i] = v.x; w[i + 1] = v.y;
             }
         } else {
 #pragma unroll
             for (int i = 0; i < NW; ++i)
-                w[i] = *reinterpret_cast<const uint32_t *>(stage + stage_off<B>(row, 4 * (wi + i)));
+                w[i] = *reinterpret_cast<const uint32_t *>(stage + stage_off(pitch, row, 4 * (wi + i)));
         }
     } else {
         // the run starts inside a word: read NW+1 words and funnel-shift
@@ -111,7 +94,7 @@ __device__ __forceinline__ void load_run(const uint8_t *stage, int row, int code
         uint32_t src[NW + 1];
 #pragma unroll
         for (int i = 0; i <= NW; ++i)
-            src[i] = *reinterpret_cast<const uint32_t *>(stage + stage_off<B>(row, 4 * (wi + i)));
+            src[i] = *reinterpret_cast<const uint32_t *>(stage + stage_off(pitch, row, 4 * (wi + i)));
 #pragma unroll
         for (int i = 0; i < NW; ++i)
             w[i] = __funnelshift_r(src[i], src[i + 1], sh);
@@ -170,9 +153,9 @@ __device__ __forceinline__ void extract_run(const uint32_t (&w)[(R * B + 31) / 3
 #pragma unroll
         for (int i = 0; i < R / 2; ++i) {
             uint32_t v;
-            if constexpr (FLIP8)
+            if constexpr (FLIP8)   // xor the top bit of each of the two fields
                 v = lop3_and_xor(win[P::win(i)], P::mask(i),
-                                 P::magic(i) | (P::mask(i) & 0x88888888u));
+                                 P::magic(i) | (P::mask(i) & ~(P::mask(i) >> 1)));
             else
                 v = lop3_and_or(win[P::win(i)], P::mask(i), P::magic(i));
             a[i] = hsub2(v, pow2_half_bits(P::elo(i)) | (pow2_half_bits(P::ehi(i)) << 16));
@@ -200,84 +183,194 @@ __device__ __forceinline__ uint16_t s8_to_f16_bits(int v)
     return h;
 }
 
-// Stages the activations of chunks [ch0, ch0 + nch) in slot order, and the
-// per-group sums X.  MODE 0 reads fp16 x, MODE 1 int8 xq (converted exactly).
-template <int B, int R, int MODE, int MP>
-__device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t *xp, float *xs,
-                                                  int ch0, int nch, int ct)
+// Loads run `idx` (R codes of one token) of the chunks [ch0, ch0 + nch) as fp16
+// bit patterns; returns false past the end.  MODE 0 reads fp16 x, MODE 1 int8 xq
+// (converted exactly).
+template <int R, int MODE>
+__device__ __forceinline__ void load_act_run(const GemvParams &p, int ch0, int runs_per_tok,
+                                             int idx, uint16_t (&v)[R])
 {
     constexpr int G = 4 * R;
-    constexpr int NGC = 128 / G;
-    const int M = p.M;
-    const int ngp = nch * NGC;
-    for (int idx = ct; idx < M * ngp; idx += 32 * kConsumerWarps) {
-        const int m = idx / ngp;
-        const int lg = idx - m * ngp;
-        const int grp = ch0 * NGC + lg;
-        const int lc = lg / NGC;
-        const int gi = lg - lc * NGC;
-        float sum = 0.f;
-#pragma unroll 1
-        for (int tt = 0; tt < 4; ++tt) {
-            const int k0 = grp * G + tt * R;
-            uint16_t v[R];
-            if constexpr (MODE == 0) {
+    constexpr int RPC = 128 / R;                 // runs per chunk
+    const int m = idx / runs_per_tok;
+    const int rr = idx - m * runs_per_tok;
+    const int k0 = ch0 * 128 + (rr / RPC) * 128 + ((rr % RPC) / 4) * G + (rr % 4) * R;
+    if constexpr (MODE == 0) {
 #pragma unroll
-                for (int c = 0; c < R; c += 8) {
-                    uint4 q = make_uint4(0, 0, 0, 0);
-                    if (k0 + c < p.K)
-                        q = *reinterpret_cast<const uint4 *>(p.x + static_cast<long long>(m) * p.K + k0 + c);
-                    v[c + 0] = q.x & 0xFFFF; v[c + 1] = q.x >> 16;
-                    v[c + 2] = q.y & 0xFFFF; v[c + 3] = q.y >> 16;
-                    v[c + 4] = q.z & 0xFFFF; v[c + 5] = q.z >> 16;
-                    v[c + 6] = q.w & 0xFFFF; v[c + 7] = q.w >> 16;
-                }
+        for (int c = 0; c < R; c += 8) {
+            uint4 q = make_uint4(0, 0, 0, 0);
+            if (k0 + c < p.K)
+                q = *reinterpret_cast<const uint4 *>(p.x + static_cast<long long>(m) * p.K + k0 + c);
+            v[c + 0] = q.x & 0xFFFF; v[c + 1] = q.x >> 16;
+            v[c + 2] = q.y & 0xFFFF; v[c + 3] = q.y >> 16;
+            v[c + 4] = q.z & 0xFFFF; v[c + 5] = q.z >> 16;
+            v[c + 6] = q.w & 0xFFFF; v[c + 7] = q.w >> 16;
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < R; c += 8) {
+            uint2 q = make_uint2(0, 0);
+            if (k0 + c < p.K)
+                q = *reinterpret_cast<const uint2 *>(p.xq + static_cast<long long>(m) * p.K + k0 + c);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t word = e < 4 ? q.x : q.y;
+                v[c + e] = s8_to_f16_bits(static_cast<int>(static_cast<int8_t>((word >> (8 * (e & 3))) & 0xFF)));
+            }
+        }
+    }
+}
+
+// Stages the activations of chunks [ch0, ch0 + nch) in slot order and the
+// per-group sums X[group][token] (added run by run in k order, so the result
+// does not depend on the thread layout).  All consumer threads take part; two
+// runs per thread are in flight at a time.  Ends with the consumers in sync.
+template <int B, int R, int MODE>
+__device__ __forceinline__ void scatter_activations(const GemvParams &p, uint16_t *xp, float *rs,
+                                                    int ch0, int nch, int ct, bool release_producer)
+{
+    constexpr int RPC = 128 / R;
+    constexpr int NGC = 128 / (4 * R);
+    constexpr int kCT = 32 * kConsumerWarps;
+    constexpr int U = R >= 32 ? 2 : 4;           // runs in flight per thread
+    const int M = p.M;
+    const int runs_per_tok = nch * RPC;
+    const int nruns = M * runs_per_tok;
+    for (int base = ct; base < nruns || (release_producer && base == ct); base += U * kCT) {
+        uint16_t v[U][R];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (base + u * kCT < nruns)
+                load_act_run<R, MODE>(p, ch0, runs_per_tok, base + u * kCT, v[u]);
+        if (release_producer && base == ct)
+            named_arrive(2, kThreads);   // first loads issued: let the weight stream start
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int idx = base + u * kCT;
+            if (idx < nruns) {
+                const int m = idx / runs_per_tok;
+                const int rr = idx - m * runs_per_tok;
+                const int lc = rr / RPC;
+                const int gi = (rr % RPC) / 4;
+                const int tt = rr % 4;
+                float sum = 0.f;
 #pragma unroll
                 for (int c = 0; c < R; ++c)
-                    sum += f16_bits_to_f32(v[c]);
-            } else {
-                int isum = 0;
+                    sum += f16_bits_to_f32(v[u][c]);   // exact for int8 inputs
 #pragma unroll
-                for (int c = 0; c < R; c += 8) {
-                    uint2 q = make_uint2(0, 0);
-                    if (k0 + c < p.K)
-                        q = *reinterpret_cast<const uint2 *>(p.xq + static_cast<long long>(m) * p.K + k0 + c);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const uint32_t word = e < 4 ? q.x : q.y;
-                        const int val = static_cast<int>(static_cast<int8_t>((word >> (8 * (e & 3))) & 0xFF));
-                        v[c + e] = s8_to_f16_bits(val);
-                        isum += val;
-                    }
+                for (int j = 0; j < R / 4; ++j) {
+                    uint2 o;
+                    o.x = v[u][code_of_slot<B, R>(4 * j + 0)] | (static_cast<uint32_t>(v[u][code_of_slot<B, R>(4 * j + 1)]) << 16);
+                    o.y = v[u][code_of_slot<B, R>(4 * j + 2)] | (static_cast<uint32_t>(v[u][code_of_slot<B, R>(4 * j + 3)]) << 16);
+                    const int jj = gi * (R / 4) + j;
+                    *reinterpret_cast<uint2 *>(xp + ((static_cast<long long>(lc) * 8 + jj) * M + m) * 16 + tt * 4) = o;
                 }
-                sum += static_cast<float>(isum);  // exact: |sum| <= 128 * 127
+                rs[idx] = sum;
             }
-#pragma unroll
-            for (int j = 0; j < R / 4; ++j) {
-                uint2 o;
-                o.x = v[code_of_slot<B, R>(4 * j + 0)] | (static_cast<uint32_t>(v[code_of_slot<B, R>(4 * j + 1)]) << 16);
-                o.y = v[code_of_slot<B, R>(4 * j + 2)] | (static_cast<uint32_t>(v[code_of_slot<B, R>(4 * j + 3)]) << 16);
-                const int jj = gi * (R / 4) + j;
-                *reinterpret_cast<uint2 *>(xp + ((static_cast<long long>(lc) * 8 + jj) * M + m) * 16 + tt * 4) = o;
-            }
+        }
+    }
+}
+
+// Per-group sums X[group][token] from the run sums, added in k order (so the
+// result does not depend on the thread layout).  Starts and ends with the
+// consumers in sync.
+template <int R, int MP>
+__device__ __forceinline__ void group_sums(const GemvParams &p, float *xs, const float *rs,
+                                           int nch, int ct)
+{
+    constexpr int RPC = 128 / R;
+    constexpr int NGC = 128 / (4 * R);
+    constexpr int kCT = 32 * kConsumerWarps;
+    const int M = p.M;
+    const int runs_per_tok = nch * RPC;
+    named_sync(1, kCT);
+    const int ngp = nch * NGC;
+    for (int idx = ct; idx < MP * ngp; idx += kCT) {
+        const int m = idx / ngp;
+        const int lg = idx - m * ngp;
+        float sum = 0.f;
+        if (m < M) {
+            const float *r4 = rs + m * runs_per_tok + lg * 4;
+            sum = ((r4[0] + r4[1]) + r4[2]) + r4[3];
         }
         xs[lg * MP + m] = sum;
     }
-    for (int idx = ct; idx < (MP - M) * ngp; idx += 32 * kConsumerWarps) {
-        const int mm = M + idx / ngp;
-        const int lg = idx % ngp;
-        xs[lg * MP + mm] = 0.f;
+    named_sync(1, kCT);
+}
+
+template <int B, int R, int MODE, int MP>
+__device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t *xp, float *xs,
+                                                  float *rs, int ch0, int nch, int ct)
+{
+    scatter_activations<B, R, MODE>(p, xp, rs, ch0, nch, ct, false);
+    group_sums<R, MP>(p, xs, rs, nch, ct);
+}
+
+// Scales and zero*scale of the block's rows as float2 (s, z*s), loaded in
+// rounds of eight per thread so that the loads of a round are in flight
+// together.
+struct ScaleRound {
+    uint16_t s[8];
+    uint8_t z[8];
+};
+
+__device__ __forceinline__ void load_scale_round(const GemvParams &p, ScaleRound &r, int row0,
+                                                 int n, int base)
+{
+    constexpr int kCT = 32 * kConsumerWarps;
+    const int ng = p.ng;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int idx = base + u * kCT;
+        r.s[u] = 0;
+        r.z[u] = static_cast<uint8_t>(p.zero_const);
+        if (idx < n) {
+            const int rr = idx / ng;
+            const long long off = static_cast<long long>(row0 + rr) * ng + (idx - rr * ng);
+            r.s[u] = p.scales[off];
+            if (p.zeros)
+                r.z[u] = p.zeros[off];
+        }
+    }
+}
+
+__device__ __forceinline__ void store_scale_round(const GemvParams &p, float2 *sz,
+                                                  const ScaleRound &r, int n, int base)
+{
+    constexpr int kCT = 32 * kConsumerWarps;
+    const int ng = p.ng;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int idx = base + u * kCT;
+        if (idx < n) {
+            const int rr = idx / ng;
+            const float sc = f16_bits_to_f32(r.s[u]);
+            sz[rr * p.sz_pitch + (idx - rr * ng)] = make_float2(sc, static_cast<float>(r.z[u]) * sc);
+        }
+    }
+}
+
+__device__ __forceinline__ void stage_scales(const GemvParams &p, float2 *sz, int row0,
+                                             int rows_valid, int ct, int first_base)
+{
+    constexpr int kCT = 32 * kConsumerWarps;
+    const int n = rows_valid * p.ng;
+    for (int base = first_base; base < n; base += 8 * kCT) {
+        ScaleRound r;
+        load_scale_round(p, r, row0, n, base);
+        store_scale_round(p, sz, r, n, base);
     }
 }
 
 template <int B, int NT, int R, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-skinny_kernel(const __grid_constant__ CUtensorMap tmap, const GemvParams p)
+skinny_kernel(const GemvParams p)
 {
     constexpr int MP = 8 * NT;                 // padded token count of the D fragments
     constexpr int NGC = 128 / (4 * R);         // groups per 128-code chunk
-    constexpr int MAXT = NT <= 2 ? 8 : 16 / NT;   // 16-row tiles per block
-    constexpr int CS = Width<B>::CS;
+    // 16-row tiles per row block: two keeps the unrolled loop body small enough
+    // for the instruction cache (eight tiles of unrolled code thrash it)
+    constexpr int MAXT = 2;
     constexpr bool FLIP8 = (MODE == 1);
 
     extern __shared__ uint8_t smem_raw[];
@@ -290,6 +383,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmap, const GemvParams p)
     float *xs = reinterpret_cast<float *>(smem + p.off_xs);        // [group][MP]
     float2 *sz = reinterpret_cast<float2 *>(smem + p.off_sz);      // [row][sz_pitch] (s, z*s)
     float *red = reinterpret_cast<float *>(smem + p.off_red);      // [warp][rbp][MP]
+    float *rs = red;      // run sums while activations are staged (red is idle then)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -305,15 +399,21 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmap, const GemvParams p)
             mbar_init(&empty[i], kConsumerWarps);
         }
         fence_barrier_init();
+        // the next kernel on the stream may start its own set-up now; it reads
+        // nothing of ours before its griddepcontrol.wait
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
     __syncthreads();
+    // every input may have been written by the previous kernel on the stream
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == 0) {
         // ================= producer =================
+        // the consumers first issue their own small loads (scales, activations)
+        // so that those are not queued behind the weight stream
+        named_sync(2, kThreads);
         bool ok = true;
         int issued = 0;
-        if (p.use_tma && lane == 0)
-            prefetch_tmap(&tmap);
         for (int it = 0; it < total_stages && ok; ++it) {
             const int slot = it % p.ring;
             const int round = it / p.ring;
@@ -324,23 +424,25 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmap, const GemvParams p)
             const int blk = it / p.stages_per_block;
             const int s = it - blk * p.stages_per_block;
             const int row0 = r0 + blk * p.rb;
+            const int rows_here = min(p.rb, r0 + nrows - row0);
+            const long long seg_off = static_cast<long long>(s) * p.seg_bytes;
+            const int seg_len = static_cast<int>(min(static_cast<long long>(p.seg_bytes), p.row_bytes - seg_off));
             uint8_t *dst = ring + static_cast<size_t>(slot) * p.stage_bytes;
-            if (p.use_tma) {
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&full[slot], p.tile_bytes);
-                    tma_load_2d(dst, &tmap, &full[slot], s * Width<B>::ROW_BYTES, row0);
-                }
+            const uint8_t *src = p.packed + static_cast<long long>(row0) * p.row_bytes + seg_off;
+            if (p.use_bulk) {
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(rows_here * seg_len));
+                __syncwarp();
+                for (int r = lane; r < rows_here; r += 32)
+                    bulk_load(dst + r * p.pitch, src + static_cast<long long>(r) * p.row_bytes, seg_len, &full[slot]);
             } else {
-                // plain 4-byte copies (row pitch of the packed matrix not 16-byte aligned)
-                const int words_per_row = Width<B>::ROW_BYTES / 4;
-                for (int e = lane; e < p.rb * words_per_row; e += 32) {
-                    const int r = e / words_per_row;
-                    const int wo = e - r * words_per_row;
-                    const long long byte = static_cast<long long>(s) * Width<B>::ROW_BYTES + 4 * wo;
-                    uint32_t v = 0;
-                    if (row0 + r < p.N && byte < p.row_bytes)
-                        v = *reinterpret_cast<const uint32_t *>(p.packed + static_cast<long long>(row0 + r) * p.row_bytes + byte);
-                    *reinterpret_cast<uint32_t *>(dst + stage_off<B>(r, 4 * wo)) = v;
+                // plain 4-byte copies (packed rows not 16-byte aligned)
+                const int words = seg_len / 4;
+                for (int e = lane; e < rows_here * words; e += 32) {
+                    const int r = e / words;
+                    const int wo = e - r * words;
+                    *reinterpret_cast<uint32_t *>(dst + r * p.pitch + 4 * wo) =
+                        *reinterpret_cast<const uint32_t *>(src + static_cast<long long>(r) * p.row_bytes + 4 * wo);
                 }
                 __syncwarp();
                 if (lane == 0)
@@ -366,9 +468,6 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmap, const GemvParams p)
     const int ng = p.ng;
     constexpr int kCT = 32 * kConsumerWarps;
 
-    if (p.nphases == 1)
-        stage_activations<B, R, MODE, MP>(p, xp, xs, 0, p.nchunks, ct);
-
     bool ok = true;
     int it = 0;
     for (int blk = 0; blk < nblocks; ++blk) {
@@ -376,16 +475,24 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmap, const GemvParams p)
         const int rows_valid = min(p.rb, r0 + nrows - row0);
         const int T = (rows_valid + 15) / 16;
 
-        named_sync(1, kCT);   // the previous block's epilogue is done with sz / red
-        for (int idx = ct; idx < rows_valid * ng; idx += kCT) {
-            const int r = idx / ng;
-            const int grp = idx - r * ng;
-            const long long off = static_cast<long long>(row0 + r) * ng + grp;
-            const float s = f16_bits_to_f32(p.scales[off]);
-            const float z = p.zeros ? static_cast<float>(p.zeros[off]) : static_cast<float>(p.zero_const);
-            sz[r * p.sz_pitch + grp] = make_float2(s, z * s);
+        if (blk == 0 && p.nphases == 1) {
+            // first block: the first round of scale loads and the activation
+            // loads are in flight together (ahead of the weight stream); one
+            // barrier for both
+            ScaleRound r0;
+            load_scale_round(p, r0, row0, rows_valid * ng, ct);
+            scatter_activations<B, R, MODE>(p, xp, rs, 0, p.nchunks, ct, true);
+            store_scale_round(p, sz, r0, rows_valid * ng, ct);
+            stage_scales(p, sz, row0, rows_valid, ct, ct + 8 * kCT);
+            group_sums<R, MP>(p, xs, rs, p.nchunks, ct);   // starts and ends in sync
+        } else {
+            if (blk > 0)
+                named_sync(1, kCT);   // the previous block's epilogue is done with sz / red
+            else
+                named_arrive(2, kThreads);   // release the weight stream
+            stage_scales(p, sz, row0, rows_valid, ct, ct);
+            named_sync(1, kCT);
         }
-        named_sync(1, kCT);
 
         float tot[MAXT][NT][4];
 #pragma unroll
@@ -398,12 +505,11 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmap, const GemvParams p)
 
         int cur_phase = p.nphases == 1 ? 0 : -1;
         for (int s = 0; s < p.stages_per_block; ++s, ++it) {
-            const int phase = (s * CS) / p.phase_chunks;
+            const int phase = (s * p.seg_chunks) / p.phase_chunks;
             if (phase != cur_phase) {
                 named_sync(1, kCT);   // everyone is done with the previous phase
                 const int ch0 = phase * p.phase_chunks;
-                stage_activations<B, R, MODE, MP>(p, xp, xs, ch0, min(p.phase_chunks, p.nchunks - ch0), ct);
-                named_sync(1, kCT);
+                stage_activations<B, R, MODE, MP>(p, xp, xs, rs, ch0, min(p.phase_chunks, p.nchunks - ch0), ct);
                 cur_phase = phase;
             }
             const int slot = it % p.ring;
@@ -411,13 +517,12 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmap, const GemvParams p)
                 ok = mbar_wait(&full[slot], (it / p.ring) & 1, p.status);
             if (ok) {
                 const uint8_t *stage = ring + static_cast<size_t>(slot) * p.stage_bytes;
+                // this warp's chunks of the stage: cg = cw (mod 8)
+                const int cg_first = s * p.seg_chunks + ((cw - s * p.seg_chunks) & (kConsumerWarps - 1));
+                const int cg_end = min((s + 1) * p.seg_chunks, p.nchunks);
 #pragma unroll 1
-                for (int ci = 0; ci < CS; ++ci) {
-                    const int cg = s * CS + ci;
-                    if (cg >= p.nchunks)
-                        break;
-                    if ((cg & (kConsumerWarps - 1)) != cw)
-                        continue;
+                for (int cg = cg_first; cg < cg_end; cg += kConsumerWarps) {
+                    const int ci = cg - s * p.seg_chunks;
                     const int lc = cg - phase * p.phase_chunks;   // chunk within the phase
 #pragma unroll 1
                     for (int gi = 0; gi < NGC; ++gi) {
@@ -447,8 +552,8 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmap, const GemvParams p)
                             if (mt < T) {
                                 const int lr0 = mt * 16 + g;
                                 uint32_t w0[(R * B + 31) / 32], w1[(R * B + 31) / 32];
-                                load_run<B, R>(stage, lr0, code0, w0);
-                                load_run<B, R>(stage, lr0 + 8, code0, w1);
+                                load_run<B, R>(stage, p.pitch, lr0, code0, w0);
+                                load_run<B, R>(stage, p.pitch, lr0 + 8, code0, w1);
                                 uint32_t a0[R / 2], a1[R / 2];
                                 extract_run<B, R, FLIP8>(w0, a0);
                                 extract_run<B, R, FLIP8>(w1, a1);
@@ -456,7 +561,9 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmap, const GemvParams p)
                                 const float2 sz1 = sz[(lr0 + 8) * p.sz_pitch + grp];
 #pragma unroll
                                 for (int nt = 0; nt < NT; ++nt) {
+                                    // two independent accumulator chains (even / odd j)
                                     float d[4] = {0.f, 0.f, 0.f, 0.f};
+                                    float d2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                                     for (int j = 0; j < R / 4; ++j) {
                                         uint32_t b0, b1;
@@ -471,8 +578,14 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmap, const GemvParams p)
                                             b0 = v.x;
                                             b1 = v.y;
                                         }
-                                        mma_f16_16816(d, a0[2 * j], a1[2 * j], a0[2 * j + 1], a1[2 * j + 1], b0, b1);
+                                        if (j & 1)
+                                            mma_f16_16816(d2, a0[2 * j], a1[2 * j], a0[2 * j + 1], a1[2 * j + 1], b0, b1);
+                                        else
+                                            mma_f16_16816(d, a0[2 * j], a1[2 * j], a0[2 * j + 1], a1[2 * j + 1], b0, b1);
                                     }
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e)
+                                        d[e] += d2[e];
                                     const float2 xv = *reinterpret_cast<const float2 *>(xs + lg * MP + 8 * nt + 2 * t);
                                     if constexpr (MODE == 0) {
                                         tot[mt][nt][0] = fmaf(-sz0.y, xv.x, fmaf(sz0.x, d[0], tot[mt][nt][0]));
@@ -547,8 +660,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tmap, const GemvParams p)
 
 // ---- host-side launch of one instantiation ----------------------------------------------
 template <int B, int NT, int R, int MODE>
-cudaError_t launch_skinny(const CUtensorMap &tmap, const GemvParams &p, int grid, int smem,
-                          cudaStream_t stream)
+cudaError_t launch_skinny(const GemvParams &p, int grid, int smem, cudaStream_t stream)
 {
     auto kern = skinny_kernel<B, NT, R, MODE>;
     static int configured[64] = {0};
@@ -562,20 +674,31 @@ cudaError_t launch_skinny(const CUtensorMap &tmap, const GemvParams &p, int grid
             return e;
         configured[dev] = smem;
     }
-    kern<<<grid, kThreads, smem, stream>>>(tmap, p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+    if (e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 
 template <int B, int MODE>
-cudaError_t launch_skinny_width(const CUtensorMap &tmap, const GemvParams &p, int grid, int smem,
-                                cudaStream_t stream)
+cudaError_t launch_skinny_width(const GemvParams &p, int grid, int smem, cudaStream_t stream)
 {
-    const int nt = (p.M + 7) / 8;
+    const int nt = p.M <= 8 ? 1 : p.M <= 16 ? 2 : p.M <= 32 ? 4 : 8;   // as skinny_plan
 #define QMM_R(NTV)                                                                          \
     switch (p.group) {                                                                      \
-    case 32: return launch_skinny<B, NTV, 8, MODE>(tmap, p, grid, smem, stream);            \
-    case 64: return launch_skinny<B, NTV, 16, MODE>(tmap, p, grid, smem, stream);           \
-    default: return launch_skinny<B, NTV, 32, MODE>(tmap, p, grid, smem, stream);           \
+    case 32: return launch_skinny<B, NTV, 8, MODE>(p, grid, smem, stream);            \
+    case 64: return launch_skinny<B, NTV, 16, MODE>(p, grid, smem, stream);           \
+    default: return launch_skinny<B, NTV, 32, MODE>(p, grid, smem, stream);           \
     }
     if (nt <= 1) { QMM_R(1) }
     if (nt <= 2) { QMM_R(2) }

@@ -15,10 +15,9 @@
 
 namespace qmm {
 
-cudaError_t w4a8_launch(const CUtensorMap &tmap, const GemvParams &p, int grid, int smem,
-                        cudaStream_t stream)
+cudaError_t w4a8_launch(const GemvParams &p, int grid, int smem, cudaStream_t stream)
 {
-    return launch_skinny_width<4, 1>(tmap, p, grid, smem, stream);
+    return launch_skinny_width<4, 1>(p, grid, smem, stream);
 }
 
 qmm_status w4a8_dispatch(const int8_t *xq, const void *sa, const uint8_t *w4, const void *ws,
@@ -47,13 +46,8 @@ qmm_status w4a8_dispatch(const int8_t *xq, const void *sa, const uint8_t *w4, co
     qmm_status st = skinny_plan(p, 4, num_sms, smem_optin, &grid, &smem);
     if (st != QMM_OK)
         return st;
-    CUtensorMap tmap;
-    std::memset(&tmap, 0, sizeof(tmap));
-    p.use_tma = 0;
-    if (p.row_bytes % 16 == 0 &&
-        encode_byte_tmap(&tmap, w4, p.row_bytes, N, 16 * 4 * skinny_stage_chunks(4), p.rb, false))
-        p.use_tma = 1;
-    return w4a8_launch(tmap, p, grid, smem, stream) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+    p.use_bulk = (reinterpret_cast<uintptr_t>(w4) % 16 == 0) && (p.row_bytes % 16 == 0);
+    return w4a8_launch(p, grid, smem, stream) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
 }
 
 }  // namespace qmm
