@@ -254,6 +254,82 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+
+def time_graph(torch, stream, launches, reps: int = 10):
+    """Per-launch device time (ms) of `launches` (closures) captured in one CUDA
+    graph and replayed `reps` times; inputs rotate inside `launches`."""
+    with torch.cuda.stream(stream):
+        for f in launches:
+            f()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for f in launches:
+            f()
+    g.replay()
+    stream.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+    stream.synchronize()
+    return a.elapsed_time(b) / (reps * len(launches))
+
+
+def measure_others(torch, q, dev, stream, peak_gbs, peak_tf):
+    """The other workload families, timed the same way on device-generated
+    inputs of the workloads' shapes and laws (the values do not change the
+    work): skinny decode (M = 16, N = 14336, b = 6, group 64), the tiled path
+    (M = 128 / 512 / 2048, K = 8192, N = 28672, int4, bf16) and W4A8
+    (M = 1 / 16 / 64, K = N = 4096)."""
+    out = {}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+
+    def codes(n, k, bits):
+        return torch.randint(0, 1 << bits, (n, k), dtype=torch.uint8, device=dev, generator=gen)
+
+    def scales(n, ng):
+        return (0.02 * torch.randn(n, ng, device=dev, generator=gen).abs() + 1e-3).half()
+
+    # skinny: M=16, N=14336, b=6, group 64, uint8 zeros
+    M, N, K, b, G = 16, 14336, 4096, 6, 64
+    sets = [(q.qmm_pack(codes(N, K, b), b), scales(N, K // G), codes(N, K // G, b)) for _ in range(4)]
+    x = torch.randn(M, K, device=dev, generator=gen).half()
+    y = torch.empty(M, N, dtype=torch.float16, device=dev)
+    ms = time_graph(torch, stream, [lambda s=s_: q.qmm_gemv(x, s[0], b, G, s[1], s[2], out=y) for s_ in sets])
+    nbytes = N * K * b // 8 + N * (K // G) * 3 + M * K * 2 + M * N * 2
+    out["skinny_M16_N14336_b6_g64"] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
+                                       "frac_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4)}
+    del sets
+    # tiled: K=8192, N=28672, int4 group 128, z=8, bf16
+    N, K = 28672, 8192
+    wsets = [(q.qmm_pack(codes(N, K, 4), 4), scales(N, K // 128)) for _ in range(2)]
+    for M in (128, 512, 2048):
+        x = torch.randn(M, K, device=dev, generator=gen).bfloat16()
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        ms = time_graph(torch, stream, [lambda w=w_: q.qmm_gemm(x, w[0], 4, 128, w[1], None, 8, out=y)
+                                        for w_ in wsets], reps=3 if M == 2048 else 6)
+        tf = 2.0 * M * N * K / ms / 1e9
+        out[f"tiled_M{M}"] = {"us": round(ms * 1e3, 1), "TFLOPs": round(tf, 1),
+                              "frac_bf16": round(tf / peak_tf, 4)}
+    del wsets
+    # W4A8: K=N=4096, group 128
+    N = K = 4096
+    wsets = [(q.qmm_pack(codes(N, K, 4), 4), scales(N, K // 128)) for _ in range(8)]
+    for M in (1, 16, 64):
+        xq = torch.randint(-127, 128, (M, K), dtype=torch.int8, device=dev, generator=gen)
+        sa = (0.02 * torch.randn(M, device=dev, generator=gen).abs() + 1e-3).half()
+        y = torch.empty(M, N, dtype=torch.float16, device=dev)
+        ms = time_graph(torch, stream, [lambda w=w_: q.qmm_w4a8(xq, sa, w[0], w[1], 128, out=y) for w_ in wsets])
+        nbytes = N * K // 2 + N * (K // 128) * 2 + M * K + M * 2 + M * N * 2
+        out[f"w4a8_M{M}"] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
+                             "frac_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4),
+                             "TOPs": round(2.0 * M * N * K / ms / 1e9, 1)}
+    return out
+
 # ---- GPU leg -------------------------------------------------------------------------------
 def _libcuda():
     return ctypes.CDLL("libcuda.so.1")
@@ -433,6 +509,16 @@ def run_ours(args, world, rank, local):
 
     assert q.qmm_device_status(stream) == 0
 
+    others = None
+    if not args.no_others:
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+                peak_tf = float(json.load(f)["bf16_tflops"])
+        except Exception:
+            peak_tf = 1900.0
+        others = measure_others(torch, q, dev, stream, peak, peak_tf)
+        assert q.qmm_device_status(stream) == 0
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, threads, sample = oracle_baseline(OracleSweep())
@@ -467,6 +553,8 @@ def run_ours(args, world, rank, local):
         }
         if cpu is not None:
             line["cpu_baseline"] = cpu
+        if others is not None:
+            line["others"] = others
         print(json.dumps(line), flush=True)
 
 
@@ -478,6 +566,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--copies", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the timing of the other workload families")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
