@@ -25,6 +25,7 @@ struct DeviceFacts {
     qmm_status usable = QMM_ERR_DEVICE;
     int num_sms = 0;
     int smem_optin = 0;
+    int smem_pair = 0;   // per-CTA shared memory with which two CTAs share an SM
     int *status = nullptr;
 };
 
@@ -47,6 +48,10 @@ const DeviceFacts *device_facts()
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
         cudaDeviceGetAttribute(&f.num_sms, cudaDevAttrMultiProcessorCount, dev);
         cudaDeviceGetAttribute(&f.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        int smem_sm = 0, reserved = 0;
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+        f.smem_pair = (smem_sm / 2 - reserved) / 128 * 128;
         void *addr = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&addr, g_status_word);
         if (e != cudaSuccess || major != 10 || minor != 3 || f.num_sms <= 0) {
@@ -246,7 +251,7 @@ qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int
     p.zero_const = zeros ? 0 : zero_const;
     p.y_bf16 = y_dtype == QMM_BF16;
     int grid = 0, smem = 0;
-    st = skinny_plan(p, bits, f->num_sms, f->smem_optin, &grid, &smem);
+    st = skinny_plan(p, bits, f->num_sms, f->smem_optin, f->smem_pair, &grid, &smem);
     if (st != QMM_OK)
         return st;
     p.use_bulk = aligned(packed, 16) && p.row_bytes % 16 == 0;
@@ -313,7 +318,7 @@ qmm_status qmm_w4a8(const int8_t *xq, const void *sa, const uint8_t *w4, const v
         return from_cuda(e);
     }
     return w4a8_dispatch(xq, sa, w4, ws, group, y, acc_out, M, N, K, f->status, f->num_sms,
-                         f->smem_optin, stream);
+                         f->smem_optin, f->smem_pair, stream);
 }
 
 qmm_status qmm_device_status(cudaStream_t stream)

@@ -1,5 +1,5 @@
 // gemv.cu -- host planning for the skinny kernel (shared by qmm_gemv and
-// qmm_w4a8): grid, row blocks, K phases and the shared-memory layout.
+// qmm_w4a8): grid, row blocks, K segments and phases, shared-memory layout.
 #include "gemv.h"
 #include "skinny.cuh"
 
@@ -7,50 +7,45 @@ namespace qmm {
 
 static int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
-// pipeline stages in flight per CTA
-constexpr int kLookahead = 3;
+// shortest per-row segment (bytes) tried before falling back to anything that fits
+constexpr int kMinSegBytes = 256;
+// most pipeline slots per CTA
+constexpr int kMaxRing = 16;
 
 // n-tiles of 8 tokens the kernel is instantiated with (1, 2, 4 or 8)
 static int token_tiles(int M) { return M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8; }
 
-// Lays out shared memory for row blocks of `rb` rows and K phases of `cp`
-// chunks; returns the dynamic shared-memory size, or 0 if it does not fit with
-// at least `min_ring` pipeline stages.
-static int plan_smem(GemvParams &p, int bits, int rb, int cp, int smem_max, int min_ring)
+// Lays out shared memory for row blocks of `rb` rows, K phases of `cp` chunks and
+// at most `max_ring` slots; returns the dynamic shared-memory size, or 0 if
+// fewer than `min_ring` slots fit in `budget` bytes.
+static int plan_layout(GemvParams &p, int rb, int cp, int budget, int max_ring, int min_ring)
 {
-    const int nt = token_tiles(p.M);
-    const int MP = 8 * nt;
+    const int MP = 8 * token_tiles(p.M);
     const int ngc = 128 / p.group;
     p.rb = rb;
     p.rbp = align_up(rb, 16);
     p.phase_chunks = cp;
     p.nphases = (p.nchunks + cp - 1) / cp;
-    p.stage_bytes = align_up(p.rbp * p.pitch + 16, 128);
-    p.sz_pitch = p.ng + ((p.ng & 1) ? 0 : 1);
-    const int x_bytes = align_up(p.M * cp * 128 * 2, 16);
-    const int xs_bytes = align_up(cp * ngc * MP * 4, 16);
-    const int sz_bytes = align_up(p.rbp * p.sz_pitch * 8, 16);
-    // the reduction buffer also holds the per-run activation sums while staging
-    const int runsum_bytes = p.M * cp * (128 / (p.group / 4)) * 4;
-    int red_bytes = align_up(kConsumerWarps * p.rbp * MP * 4, 16);
-    if (red_bytes < align_up(runsum_bytes, 16))
-        red_bytes = align_up(runsum_bytes, 16);
-    const int fixed = x_bytes + xs_bytes + sz_bytes + red_bytes;
-    const int budget = smem_max - 1024 /* alignment slack */ - fixed;
-    if (budget <= 0)
+    // a slot holds rb rows; the MMA tiles also read the rows up to rbp, whose
+    // results are dropped: those reads land in the slack at the end
+    p.stage_bytes = align_up(rb * p.pitch, 128);
+    const int overrun = align_up((p.rbp - rb) * p.pitch + 16, 128);
+    p.sz_pitch = p.ng + ((p.ng & 1) ? 0 : 1);   // odd: the eight rows of a tile hit different banks
+    const int bar_bytes = align_up(kMaxRing * 12, 128);
+    const int x_bytes = align_up(p.M * cp * 128 * 2, 128);
+    const int xs_bytes = align_up(cp * ngc * MP * 4, 128);
+    const int sz_bytes = align_up(p.rbp * p.sz_pitch * (p.zeros ? 3 : 2), 128);
+    const int red_bytes = align_up((1 << p.ksplit_log2) * p.rbp * MP * 4, 128);
+    const int fixed = 128 /* base alignment */ + bar_bytes + x_bytes + xs_bytes + sz_bytes + red_bytes + overrun;
+    if (budget - fixed < p.stage_bytes * min_ring)
         return 0;
-    // A few stages of look-ahead keep enough bytes in flight for HBM while
-    // letting the stages land roughly in order (issuing a whole block at once
-    // makes every stage complete near the end, so compute cannot overlap).
-    int ring = budget / (p.stage_bytes + 16);
-    if (ring > kLookahead)
-        ring = kLookahead;
-    if (ring < min_ring)
-        return 0;
+    int ring = (budget - fixed) / p.stage_bytes;
+    if (ring > max_ring)
+        ring = max_ring;
     p.ring = ring;
-    int off = ring * p.stage_bytes;
+    int off = 0;
     p.off_bar = off;
-    off += align_up(2 * ring * 8, 16);
+    off += bar_bytes;
     p.off_x = off;
     off += x_bytes;
     p.off_xs = off;
@@ -59,15 +54,28 @@ static int plan_smem(GemvParams &p, int bits, int rb, int cp, int smem_max, int 
     off += sz_bytes;
     p.off_red = off;
     off += red_bytes;
-    return off + 1024;
+    p.off_ring = off;
+    off += ring * p.stage_bytes + overrun;
+    return off + 128;
 }
 
-qmm_status skinny_plan(GemvParams &p, int bits, int num_sms, int smem_max, int *grid_out,
-                       int *smem_out)
+// Sets the K segment of `seg` chunks (pitch: 16*b mod 128, or 16 for b = 8, so
+// that the four threads of a quad and the eight rows of a tile read distinct
+// banks).
+static void set_segment(GemvParams &p, int bits, int seg)
+{
+    p.seg_chunks = seg;
+    p.seg_bytes = seg * 16 * bits;
+    const int want = bits == 8 ? 16 : (16 * bits) % 128;
+    const int pad = ((want - p.seg_bytes % 128) % 128 + 128) % 128;
+    p.pitch = p.seg_bytes + pad;
+    p.stages_per_block = (p.nchunks + seg - 1) / seg;
+}
+
+qmm_status skinny_plan(GemvParams &p, int bits, int num_sms, int smem_max, int smem_pair,
+                       int *grid_out, int *smem_out)
 {
     p.nchunks = (p.K + 127) / 128;
-    const int maxt = 2;   // as the kernel's MAXT
-    const int rbmax = 16 * maxt;
     int grid = (p.N + 15) / 16;
     if (grid > num_sms)
         grid = num_sms;
@@ -76,41 +84,74 @@ qmm_status skinny_plan(GemvParams &p, int bits, int num_sms, int smem_max, int *
     p.rows_base = p.N / grid;
     p.rows_rem = p.N % grid;
     const int rows_max = p.rows_base + (p.rows_rem ? 1 : 0);
-    // K segment: about a kilobyte of each row per stage, at least 8 chunks;
-    // smaller when the activations of a segment do not fit (large M)
+    // a block holds at most 8 tiles of 16 rows (two per warp of a K split of 2)
+    const int rbmax = 16 * kWarps * kTilesPerWarp / 2;
+    const int nblk0 = (rows_max + rbmax - 1) / rbmax;
+    // K segment: about a kilobyte of each row per stage, at least 8 chunks
     int seg0 = (1024 + 16 * bits - 1) / (16 * bits);
     if (seg0 < 8)
         seg0 = 8;
     if (seg0 > p.nchunks)
         seg0 = p.nchunks;
-    for (int seg = seg0; seg >= 1; seg = seg > 1 ? seg / 2 : 0) {
-        p.seg_chunks = seg;
-        p.seg_bytes = seg * 16 * bits;
-        // pitch = 16*b (mod 128), or 16 for b = 8: with it the four threads of a
-        // quad and the eight rows of an MMA tile read distinct banks
-        const int want = bits == 8 ? 16 : (16 * bits) % 128;
-        const int pad = ((want - p.seg_bytes % 128) % 128 + 128) % 128;
-        p.pitch = p.seg_bytes + pad;
-        p.stages_per_block = (p.nchunks + seg - 1) / seg;
-        const int cp_full = p.stages_per_block * seg;
-        for (int nblk = (rows_max + rbmax - 1) / rbmax; nblk <= rows_max; ++nblk) {
-            const int rb = (rows_max + nblk - 1) / nblk;
-            // prefer one activation phase; otherwise the largest phase that fits
-            for (int cp = cp_full; cp >= seg; cp = (cp / 2 / seg) * seg) {
-                const int smem = plan_smem(p, bits, rb, cp, smem_max, 2);
-                if (smem) {
-                    *grid_out = grid;
-                    *smem_out = smem;
-                    return QMM_OK;
+    const int budgets[2] = {smem_pair, smem_max};
+    // Preference: a layout that lets two CTAs share an SM (if it needs no more
+    // phases or blocks than the smallest); then one activation phase; fewer row blocks (a block switch drains the pipeline); then the
+    // most bytes in flight, with longer segments unless a shorter one keeps at
+    // least 15% more in flight.  Segments under kMinSegBytes come last.
+    for (int bi = 0; bi < 2; ++bi) {
+        const int budget = budgets[bi];
+        if (budget <= 0 || budget > smem_max)
+            continue;
+        // sharing an SM is taken only without extra phases, row blocks or short segments
+        const int nph_max = bi == 0 ? 1 : p.nchunks;
+        const int nblk_max = bi == 0 ? nblk0 : nblk0 + 4;
+        for (int pass = 0; pass < (bi == 0 ? 1 : 2); ++pass) {
+            for (int nph = 1; nph <= nph_max; ++nph) {
+                for (int nblk = nblk0; nblk <= nblk_max; ++nblk) {
+                    const int rb = (rows_max + nblk - 1) / nblk;
+                    // the largest K split whose tile groups cover the tiles, two per warp
+                    const int tiles = (rb + 15) / 16;
+                    int kl = 3;
+                    while (kl > 0 && tiles > kTilesPerWarp * (kWarps >> kl))
+                        --kl;
+                    p.ksplit_log2 = kl;
+                    int best_seg = 0;
+                    long long best_inflight = 0;
+                    for (int seg = seg0; seg >= 1; --seg) {
+                        if (pass == 0 && seg < seg0 && seg * 16 * bits < kMinSegBytes)
+                            break;
+                        set_segment(p, bits, seg);
+                        // phase = a whole number of segments covering nchunks in nph phases
+                        const int cp = ((p.stages_per_block + nph - 1) / nph) * seg;
+                        if ((p.nchunks + cp - 1) / cp != nph)
+                            continue;
+                        const int total = nblk * p.stages_per_block;
+                        const int max_ring = total < kMaxRing ? total : kMaxRing;
+                        if (!plan_layout(p, rb, cp, budget, max_ring, max_ring < 2 ? max_ring : 2))
+                            continue;
+                        // bytes in flight from the start: the ring, or the whole slice if less
+                        long long inflight = static_cast<long long>(p.ring) * p.seg_bytes;
+                        if (inflight > p.row_bytes * nblk)
+                            inflight = p.row_bytes * nblk;
+                        inflight *= rb;
+                        if (best_seg == 0 || inflight * 100 > best_inflight * 115) {
+                            best_seg = seg;
+                            best_inflight = inflight;
+                        }
+                    }
+                    if (best_seg) {
+                        set_segment(p, bits, best_seg);
+                        const int cp = ((p.stages_per_block + nph - 1) / nph) * best_seg;
+                        const int total = nblk * p.stages_per_block;
+                        const int max_ring = total < kMaxRing ? total : kMaxRing;
+                        const int smem = plan_layout(p, rb, cp, budget, max_ring, max_ring < 2 ? max_ring : 2);
+                        *grid_out = grid;
+                        *smem_out = smem;
+                        return QMM_OK;
+                    }
                 }
-                if (cp == seg)
-                    break;
             }
-            if (rb <= 16)
-                break;
         }
-        if (seg == 1)
-            break;
     }
     return QMM_ERR_UNSUPPORTED;
 }

@@ -33,13 +33,17 @@ struct GemvParams {
     int nphases;
     int rows_base, rows_rem;  // CTA c owns rows_base + (c < rows_rem) rows
     int rb, rbp;              // rows per block, rounded up to 16
-    int ring, stage_bytes;
-    int off_bar, off_x, off_xs, off_sz, off_red, sz_pitch;
+    int ksplit_log2;          // 8 warps = 2^ksplit_log2 K splits x (8 >> ksplit_log2) tile groups
+    int ring, stage_bytes;    // pipeline slots and the bytes of one
+    int off_bar, off_x, off_xs, off_sz, off_red, off_ring, sz_pitch;
 };
 
-// Chooses grid, row blocking, K phases and the shared-memory layout.
-// QMM_ERR_UNSUPPORTED if no layout fits.
-qmm_status skinny_plan(GemvParams &p, int bits, int num_sms, int smem_max, int *grid, int *smem);
+// Chooses grid, row blocking, K phases and the shared-memory layout.  A layout
+// of at most `smem_pair` bytes (two CTAs per SM, so that consecutive calls
+// overlap) is preferred; `smem_max` is the per-CTA limit.  QMM_ERR_UNSUPPORTED
+// if no layout fits.
+qmm_status skinny_plan(GemvParams &p, int bits, int num_sms, int smem_max, int smem_pair, int *grid,
+                       int *smem);
 
 // Per-width launchers (one translation unit each).
 cudaError_t gemv_launch_w1(const GemvParams &, int, int, cudaStream_t);

@@ -17,15 +17,22 @@
 //
 // Work split.  CTA c owns a contiguous range of output columns (rows of the
 // packed matrix) and the whole K range; rows are processed in blocks of at most
-// 16*MAXT.  Warp 0 streams the block's bitstream through a ring of shared-memory
-// stages: a stage is one K segment (SEG 128-code chunks, about a kilobyte) of
-// every row of the block, one 1-D bulk copy (TMA) per row.  Long contiguous
-// per-row copies keep HBM efficient; the rows land at a padded pitch that makes
-// the consumers' quad-strided reads bank-conflict free.  The eight consumer
-// warps split K: warp w takes every 8th chunk; their partial sums meet in
-// shared memory and are added in a fixed order (deterministic).
-// Activations are staged once per CTA (or once per K phase when M x K does not
-// fit) in "slot" order -- the order in which codes come out of the registers.
+// 128.  A block's bitstream moves through a ring of shared-memory stages: a
+// stage is one K segment of every row of the block, one 1-D bulk copy (TMA) per
+// row, landing at a padded pitch that keeps the MMA quads' reads bank-conflict
+// free.  There is no producer warp: the first ring of stages is issued at entry
+// and the last warp to finish a stage issues the stage that reuses its slot.
+// The eight warps split K (warp w takes the chunks = w mod ksplit) and the
+// block's 16-row tiles (at most two per warp); partial sums meet in shared
+// memory and are added in a fixed order (deterministic).
+//
+// Decode sequences.  A decode-size CTA uses at most half of an SM (shared
+// memory, 256 threads x 128 registers), and the kernel signals its dependents
+// at entry, so with programmatic dependent launch the next call's CTAs start
+// beside this call's and stream their weights while this call finishes.  The
+// packed weights, scales and zeros are read before the dependency wait (the
+// ABI requires that the preceding kernel on the stream does not write them);
+// only the activations wait for the preceding kernel.
 //
 // Inside a chunk each 16-row tile takes one mma.sync.m16n8k16 per 16 codes and
 // 8 tokens.  The four threads of an MMA quad own runs of R = G/4 consecutive
@@ -33,6 +40,8 @@
 // is applied in fp32.  Codes become fp16 in registers with no shared-memory
 // round trip: a LOP3 keeps one code in each half of a 32-bit window and sets the
 // half's exponent so that it reads 2^E + q exactly; an exact HSUB2 removes 2^E.
+// Activations are staged once per CTA (or once per K phase when M x K does not
+// fit) in "slot" order -- the order in which codes come out of the registers.
 #pragma once
 
 #include <cuda.h>
@@ -43,8 +52,9 @@
 
 namespace qmm {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kWarps = 8;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kTilesPerWarp = 2;   // 16-row tiles a warp computes per block, at most
 
 // Byte offset of (row, byte) inside a stage: rows sit at a padded pitch.
 __device__ __forceinline__ uint32_t stage_off(int pitch, int row, int byte)
@@ -221,39 +231,47 @@ __device__ __forceinline__ void load_act_run(const GemvParams &p, int ch0, int r
     }
 }
 
-// Stages the activations of chunks [ch0, ch0 + nch) in slot order and the
-// per-group sums X[group][token] (added run by run in k order, so the result
-// does not depend on the thread layout).  All consumer threads take part; two
-// runs per thread are in flight at a time.  Ends with the consumers in sync.
-template <int B, int R, int MODE>
-__device__ __forceinline__ void scatter_activations(const GemvParams &p, uint16_t *xp, float *rs,
-                                                    int ch0, int nch, int ct, bool release_producer)
+// Stages the activations of chunks [ch0, ch0 + nch) in slot order, and the
+// per-group sums X[group][token] (each run summed in k order, the four runs of a
+// group added in order across the quad's lanes: independent of the launch).
+// MP - M padded tokens get X = 0.
+template <int B, int R, int MODE, int MP>
+__device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t *xp, float *xs,
+                                                  int ch0, int nch)
 {
-    constexpr int RPC = 128 / R;
-    constexpr int NGC = 128 / (4 * R);
-    constexpr int kCT = 32 * kConsumerWarps;
-    constexpr int U = R >= 32 ? 2 : 4;           // runs in flight per thread
+    constexpr int RPC = 128 / R;                 // runs per chunk
+    constexpr int NGC = 128 / (4 * R);           // groups per chunk
+    constexpr int U = R >= 32 ? 1 : 2;           // runs in flight per thread
     const int M = p.M;
+    const int lane = threadIdx.x & 31;
     const int runs_per_tok = nch * RPC;
     const int nruns = M * runs_per_tok;
-    for (int base = ct; base < nruns || (release_producer && base == ct); base += U * kCT) {
+    if (MP > M) {
+        const int ngp = nch * NGC;
+        for (int idx = threadIdx.x; idx < ngp * (MP - M); idx += kThreads) {
+            const int lg = idx / (MP - M);
+            xs[lg * MP + M + (idx - lg * (MP - M))] = 0.f;
+        }
+    }
+    // warp-uniform trip count: the quad shuffles need every lane
+    for (int wbase = threadIdx.x - lane; wbase < nruns; wbase += U * kThreads) {
         uint16_t v[U][R];
 #pragma unroll
         for (int u = 0; u < U; ++u)
-            if (base + u * kCT < nruns)
-                load_act_run<R, MODE>(p, ch0, runs_per_tok, base + u * kCT, v[u]);
-        if (release_producer && base == ct)
-            named_arrive(2, kThreads);   // first loads issued: let the weight stream start
+            if (wbase + lane + u * kThreads < nruns)
+                load_act_run<R, MODE>(p, ch0, runs_per_tok, wbase + lane + u * kThreads, v[u]);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int idx = base + u * kCT;
-            if (idx < nruns) {
-                const int m = idx / runs_per_tok;
+            const int idx = wbase + lane + u * kThreads;
+            const bool valid = idx < nruns;   // whole quads: nruns is a multiple of 4
+            float sum = 0.f;
+            int m = 0, lc = 0, gi = 0, tt = 0;
+            if (valid) {
+                m = idx / runs_per_tok;
                 const int rr = idx - m * runs_per_tok;
-                const int lc = rr / RPC;
-                const int gi = (rr % RPC) / 4;
-                const int tt = rr % 4;
-                float sum = 0.f;
+                lc = rr / RPC;
+                gi = (rr % RPC) / 4;
+                tt = rr % 4;
 #pragma unroll
                 for (int c = 0; c < R; ++c)
                     sum += f16_bits_to_f32(v[u][c]);   // exact for int8 inputs
@@ -265,125 +283,108 @@ __device__ __forceinline__ void scatter_activations(const GemvParams &p, uint16_
                     const int jj = gi * (R / 4) + j;
                     *reinterpret_cast<uint2 *>(xp + ((static_cast<long long>(lc) * 8 + jj) * M + m) * 16 + tt * 4) = o;
                 }
-                rs[idx] = sum;
+            }
+            const float s1 = __shfl_down_sync(0xffffffffu, sum, 1);
+            const float s2 = __shfl_down_sync(0xffffffffu, sum, 2);
+            const float s3 = __shfl_down_sync(0xffffffffu, sum, 3);
+            if (valid && tt == 0)
+                xs[(lc * NGC + gi) * MP + m] = ((sum + s1) + s2) + s3;
+        }
+    }
+}
+
+// Scales (fp16 bits, as stored) and per-group zeros (uint8) of a block's rows,
+// eight loads per thread in flight; the fold converts them (exactly) at use.
+__device__ __forceinline__ void stage_scales(const GemvParams &p, uint16_t *s16, uint8_t *z8, int row0,
+                                             int rows_valid)
+{
+    const int ng = p.ng;
+    const int n = rows_valid * ng;
+    for (int base = threadIdx.x; base < n; base += 8 * kThreads) {
+        uint16_t sv[8];
+        uint8_t zv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = base + u * kThreads;
+            sv[u] = 0;
+            zv[u] = 0;
+            if (idx < n) {
+                const long long off = static_cast<long long>(row0) * ng + idx;
+                sv[u] = p.scales[off];
+                if (p.zeros)
+                    zv[u] = p.zeros[off];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = base + u * kThreads;
+            if (idx < n) {
+                const int rr = idx / ng;
+                const int o = rr * p.sz_pitch + (idx - rr * ng);
+                s16[o] = sv[u];
+                if (p.zeros)
+                    z8[o] = zv[u];
             }
         }
     }
 }
 
-// Per-group sums X[group][token] from the run sums, added in k order (so the
-// result does not depend on the thread layout).  Starts and ends with the
-// consumers in sync.
-template <int R, int MP>
-__device__ __forceinline__ void group_sums(const GemvParams &p, float *xs, const float *rs,
-                                           int nch, int ct)
+// Issues pipeline stage `it` (K segment s of row block blk) into ring slot
+// `slot`: one bulk copy per row, completing on full[slot].  Called by a whole
+// warp.  Without 16-byte aligned rows the warp copies with 4-byte loads.
+__device__ __forceinline__ void issue_stage(const GemvParams &p, int it, int slot, uint8_t *ring,
+                                            uint64_t *full, int r0, int nrows, uint64_t policy)
 {
-    constexpr int RPC = 128 / R;
-    constexpr int NGC = 128 / (4 * R);
-    constexpr int kCT = 32 * kConsumerWarps;
-    const int M = p.M;
-    const int runs_per_tok = nch * RPC;
-    named_sync(1, kCT);
-    const int ngp = nch * NGC;
-    for (int idx = ct; idx < MP * ngp; idx += kCT) {
-        const int m = idx / ngp;
-        const int lg = idx - m * ngp;
-        float sum = 0.f;
-        if (m < M) {
-            const float *r4 = rs + m * runs_per_tok + lg * 4;
-            sum = ((r4[0] + r4[1]) + r4[2]) + r4[3];
+    const int lane = threadIdx.x & 31;
+    const int blk = it / p.stages_per_block;
+    const int s = it - blk * p.stages_per_block;
+    const int row0 = r0 + blk * p.rb;
+    const int rows_here = min(p.rb, r0 + nrows - row0);
+    const long long seg_off = static_cast<long long>(s) * p.seg_bytes;
+    const int seg_len = static_cast<int>(min(static_cast<long long>(p.seg_bytes), p.row_bytes - seg_off));
+    uint8_t *dst = ring + static_cast<size_t>(slot) * p.stage_bytes;
+    const uint8_t *src = p.packed + static_cast<long long>(row0) * p.row_bytes + seg_off;
+    if (p.use_bulk) {
+        if (lane == 0)
+            mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(rows_here * seg_len));
+        __syncwarp();
+        for (int r = lane; r < rows_here; r += 32)
+            bulk_load_hint(dst + r * p.pitch, src + static_cast<long long>(r) * p.row_bytes, seg_len,
+                           &full[slot], policy);
+    } else {
+        const int words = seg_len / 4;
+        for (int e = lane; e < rows_here * words; e += 32) {
+            const int r = e / words;
+            const int wo = e - r * words;
+            *reinterpret_cast<uint32_t *>(dst + r * p.pitch + 4 * wo) =
+                *reinterpret_cast<const uint32_t *>(src + static_cast<long long>(r) * p.row_bytes + 4 * wo);
         }
-        xs[lg * MP + m] = sum;
-    }
-    named_sync(1, kCT);
-}
-
-template <int B, int R, int MODE, int MP>
-__device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t *xp, float *xs,
-                                                  float *rs, int ch0, int nch, int ct)
-{
-    scatter_activations<B, R, MODE>(p, xp, rs, ch0, nch, ct, false);
-    group_sums<R, MP>(p, xs, rs, nch, ct);
-}
-
-// Scales and zero*scale of the block's rows as float2 (s, z*s), loaded in
-// rounds of eight per thread so that the loads of a round are in flight
-// together.
-struct ScaleRound {
-    uint16_t s[8];
-    uint8_t z[8];
-};
-
-__device__ __forceinline__ void load_scale_round(const GemvParams &p, ScaleRound &r, int row0,
-                                                 int n, int base)
-{
-    constexpr int kCT = 32 * kConsumerWarps;
-    const int ng = p.ng;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        const int idx = base + u * kCT;
-        r.s[u] = 0;
-        r.z[u] = static_cast<uint8_t>(p.zero_const);
-        if (idx < n) {
-            const int rr = idx / ng;
-            const long long off = static_cast<long long>(row0 + rr) * ng + (idx - rr * ng);
-            r.s[u] = p.scales[off];
-            if (p.zeros)
-                r.z[u] = p.zeros[off];
-        }
-    }
-}
-
-__device__ __forceinline__ void store_scale_round(const GemvParams &p, float2 *sz,
-                                                  const ScaleRound &r, int n, int base)
-{
-    constexpr int kCT = 32 * kConsumerWarps;
-    const int ng = p.ng;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        const int idx = base + u * kCT;
-        if (idx < n) {
-            const int rr = idx / ng;
-            const float sc = f16_bits_to_f32(r.s[u]);
-            sz[rr * p.sz_pitch + (idx - rr * ng)] = make_float2(sc, static_cast<float>(r.z[u]) * sc);
-        }
-    }
-}
-
-__device__ __forceinline__ void stage_scales(const GemvParams &p, float2 *sz, int row0,
-                                             int rows_valid, int ct, int first_base)
-{
-    constexpr int kCT = 32 * kConsumerWarps;
-    const int n = rows_valid * p.ng;
-    for (int base = first_base; base < n; base += 8 * kCT) {
-        ScaleRound r;
-        load_scale_round(p, r, row0, n, base);
-        store_scale_round(p, sz, r, n, base);
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&full[slot]);
     }
 }
 
 template <int B, int NT, int R, int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, (NT == 1 || (NT == 2 && MODE == 0)) ? 2 : 1)
 skinny_kernel(const GemvParams p)
 {
     constexpr int MP = 8 * NT;                 // padded token count of the D fragments
     constexpr int NGC = 128 / (4 * R);         // groups per 128-code chunk
-    // 16-row tiles per row block: two keeps the unrolled loop body small enough
-    // for the instruction cache (eight tiles of unrolled code thrash it)
-    constexpr int MAXT = 2;
     constexpr bool FLIP8 = (MODE == 1);
+    constexpr int TPW = kTilesPerWarp;
 
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
-    uint8_t *ring = smem;
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                                ~static_cast<uintptr_t>(127));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
-    uint64_t *empty = full + p.ring;
+    int *done_count = reinterpret_cast<int *>(full + p.ring);       // warps done per slot (monotonic)
     uint16_t *xp = reinterpret_cast<uint16_t *>(smem + p.off_x);   // [chunk][8][M][4][4]
     float *xs = reinterpret_cast<float *>(smem + p.off_xs);        // [group][MP]
-    float2 *sz = reinterpret_cast<float2 *>(smem + p.off_sz);      // [row][sz_pitch] (s, z*s)
-    float *red = reinterpret_cast<float *>(smem + p.off_red);      // [warp][rbp][MP]
-    float *rs = red;      // run sums while activations are staged (red is idle then)
+    uint16_t *s16 = reinterpret_cast<uint16_t *>(smem + p.off_sz);  // [row][sz_pitch] fp16 scales
+    uint8_t *z8 = smem + p.off_sz + p.rbp * p.sz_pitch * 2;          // [row][sz_pitch] zeros
+    float *red = reinterpret_cast<float *>(smem + p.off_red);      // [ksplit][rbp][MP]
+    uint8_t *ring = smem + p.off_ring;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -396,77 +397,39 @@ skinny_kernel(const GemvParams p)
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.ring; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kConsumerWarps);
+            done_count[i] = 0;
         }
         fence_barrier_init();
-        // the next kernel on the stream may start its own set-up now; it reads
-        // nothing of ours before its griddepcontrol.wait
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
     __syncthreads();
-    // every input may have been written by the previous kernel on the stream
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the next kernel on the stream may start now; it reads nothing that this
+    // one writes before its own griddepcontrol.wait
+    if (threadIdx.x == 0)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+    // ---- before the dependency wait: weights and scales (not written by the
+    // preceding kernel) ----
+    const uint64_t policy = l2_evict_first_policy();   // the bitstream is read once
     if (warp == 0) {
-        // ================= producer =================
-        // the consumers first issue their own small loads (scales, activations)
-        // so that those are not queued behind the weight stream
-        named_sync(2, kThreads);
-        bool ok = true;
-        int issued = 0;
-        for (int it = 0; it < total_stages && ok; ++it) {
-            const int slot = it % p.ring;
-            const int round = it / p.ring;
-            if (round > 0)
-                ok = mbar_wait(&empty[slot], (round - 1) & 1, p.status);
-            if (!ok)
-                break;
-            const int blk = it / p.stages_per_block;
-            const int s = it - blk * p.stages_per_block;
-            const int row0 = r0 + blk * p.rb;
-            const int rows_here = min(p.rb, r0 + nrows - row0);
-            const long long seg_off = static_cast<long long>(s) * p.seg_bytes;
-            const int seg_len = static_cast<int>(min(static_cast<long long>(p.seg_bytes), p.row_bytes - seg_off));
-            uint8_t *dst = ring + static_cast<size_t>(slot) * p.stage_bytes;
-            const uint8_t *src = p.packed + static_cast<long long>(row0) * p.row_bytes + seg_off;
-            if (p.use_bulk) {
-                if (lane == 0)
-                    mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(rows_here * seg_len));
-                __syncwarp();
-                for (int r = lane; r < rows_here; r += 32)
-                    bulk_load(dst + r * p.pitch, src + static_cast<long long>(r) * p.row_bytes, seg_len, &full[slot]);
-            } else {
-                // plain 4-byte copies (packed rows not 16-byte aligned)
-                const int words = seg_len / 4;
-                for (int e = lane; e < rows_here * words; e += 32) {
-                    const int r = e / words;
-                    const int wo = e - r * words;
-                    *reinterpret_cast<uint32_t *>(dst + r * p.pitch + 4 * wo) =
-                        *reinterpret_cast<const uint32_t *>(src + static_cast<long long>(r) * p.row_bytes + 4 * wo);
-                }
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&full[slot]);
-            }
-            ++issued;
-        }
-        // drain: no copy into this CTA's shared memory may still be in flight
-        if (lane == 0) {
-            const int first = issued > p.ring ? issued - p.ring : 0;
-            for (int it = first; it < issued; ++it)
-                if (!mbar_wait(&full[it % p.ring], (it / p.ring) & 1, p.status))
-                    break;
-        }
-        return;
+        const int first = min(p.ring, total_stages);
+        for (int it = 0; it < first; ++it)
+            issue_stage(p, it, it, ring, full, r0, nrows, policy);
     }
+    stage_scales(p, s16, z8, r0, min(p.rb, nrows));
 
-    // ================= consumers =================
-    const int cw = warp - 1;              // consumer warp 0..7
-    const int ct = threadIdx.x - 32;      // consumer thread 0..255
+    // ---- the activations may come from the preceding kernel ----
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (p.nphases == 1)
+        stage_activations<B, R, MODE, MP>(p, xp, xs, 0, p.nchunks);
+    __syncthreads();
+
+    const int ksplit = 1 << p.ksplit_log2;
+    const int kid = warp & (ksplit - 1);          // K split: chunks = kid (mod ksplit)
+    const int tg = warp >> p.ksplit_log2;         // tile group: tiles tg, tg + ntg
+    const int ntg = kWarps >> p.ksplit_log2;
     const int g = lane >> 2, t = lane & 3;
     const int M = p.M;
     const int ng = p.ng;
-    constexpr int kCT = 32 * kConsumerWarps;
 
     bool ok = true;
     int it = 0;
@@ -475,41 +438,29 @@ skinny_kernel(const GemvParams p)
         const int rows_valid = min(p.rb, r0 + nrows - row0);
         const int T = (rows_valid + 15) / 16;
 
-        if (blk == 0 && p.nphases == 1) {
-            // first block: the first round of scale loads and the activation
-            // loads are in flight together (ahead of the weight stream); one
-            // barrier for both
-            ScaleRound r0;
-            load_scale_round(p, r0, row0, rows_valid * ng, ct);
-            scatter_activations<B, R, MODE>(p, xp, rs, 0, p.nchunks, ct, true);
-            store_scale_round(p, sz, r0, rows_valid * ng, ct);
-            stage_scales(p, sz, row0, rows_valid, ct, ct + 8 * kCT);
-            group_sums<R, MP>(p, xs, rs, p.nchunks, ct);   // starts and ends in sync
-        } else {
-            if (blk > 0)
-                named_sync(1, kCT);   // the previous block's epilogue is done with sz / red
-            else
-                named_arrive(2, kThreads);   // release the weight stream
-            stage_scales(p, sz, row0, rows_valid, ct, ct);
-            named_sync(1, kCT);
+        if (blk > 0) {
+            __syncthreads();   // the previous block's epilogue is done with s16 / z8 / red
+            stage_scales(p, s16, z8, row0, rows_valid);
+            __syncthreads();
         }
 
-        float tot[MAXT][NT][4];
+        float tot[TPW][NT][4];
 #pragma unroll
-        for (int mt = 0; mt < MAXT; ++mt)
+        for (int i = 0; i < TPW; ++i)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    tot[mt][nt][e] = 0.f;
+                    tot[i][nt][e] = 0.f;
 
         int cur_phase = p.nphases == 1 ? 0 : -1;
         for (int s = 0; s < p.stages_per_block; ++s, ++it) {
             const int phase = (s * p.seg_chunks) / p.phase_chunks;
             if (phase != cur_phase) {
-                named_sync(1, kCT);   // everyone is done with the previous phase
+                __syncthreads();   // everyone is done with the previous phase
                 const int ch0 = phase * p.phase_chunks;
-                stage_activations<B, R, MODE, MP>(p, xp, xs, rs, ch0, min(p.phase_chunks, p.nchunks - ch0), ct);
+                stage_activations<B, R, MODE, MP>(p, xp, xs, ch0, min(p.phase_chunks, p.nchunks - ch0));
+                __syncthreads();
                 cur_phase = phase;
             }
             const int slot = it % p.ring;
@@ -517,11 +468,11 @@ skinny_kernel(const GemvParams p)
                 ok = mbar_wait(&full[slot], (it / p.ring) & 1, p.status);
             if (ok) {
                 const uint8_t *stage = ring + static_cast<size_t>(slot) * p.stage_bytes;
-                // this warp's chunks of the stage: cg = cw (mod 8)
-                const int cg_first = s * p.seg_chunks + ((cw - s * p.seg_chunks) & (kConsumerWarps - 1));
-                const int cg_end = min((s + 1) * p.seg_chunks, p.nchunks);
+                // this warp's chunks of the stage: cg = kid (mod ksplit)
+                const int cg_first = s * p.seg_chunks + ((kid - s * p.seg_chunks) & (ksplit - 1));
+                const int cg_end = tg < T ? min((s + 1) * p.seg_chunks, p.nchunks) : 0;
 #pragma unroll 1
-                for (int cg = cg_first; cg < cg_end; cg += kConsumerWarps) {
+                for (int cg = cg_first; cg < cg_end; cg += ksplit) {
                     const int ci = cg - s * p.seg_chunks;
                     const int lc = cg - phase * p.phase_chunks;   // chunk within the phase
 #pragma unroll 1
@@ -531,7 +482,7 @@ skinny_kernel(const GemvParams p)
                             break;
                         const int lg = lc * NGC + gi;
                         const uint16_t *xb = xp + (static_cast<long long>(lc) * 8 + gi * (R / 4)) * M * 16 + t * 4;
-                        // activation fragments for the R/4 MMAs (hoisted for small NT)
+                        // activation fragments of the R/4 MMAs, shared by the warp's tiles
                         uint32_t bf[NT <= 2 ? R / 4 : 1][NT <= 2 ? NT : 1][2];
                         if constexpr (NT <= 2) {
 #pragma unroll
@@ -546,72 +497,79 @@ skinny_kernel(const GemvParams p)
                                     bf[j][nt][1] = v.y;
                                 }
                         }
+                        float2 xv[NT];
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            xv[nt] = *reinterpret_cast<const float2 *>(xs + lg * MP + 8 * nt + 2 * t);
                         const int code0 = ci * 128 + gi * 4 * R + t * R;   // within the stage row
 #pragma unroll
-                        for (int mt = 0; mt < MAXT; ++mt) {
-                            if (mt < T) {
-                                const int lr0 = mt * 16 + g;
-                                uint32_t w0[(R * B + 31) / 32], w1[(R * B + 31) / 32];
-                                load_run<B, R>(stage, p.pitch, lr0, code0, w0);
-                                load_run<B, R>(stage, p.pitch, lr0 + 8, code0, w1);
-                                uint32_t a0[R / 2], a1[R / 2];
-                                extract_run<B, R, FLIP8>(w0, a0);
-                                extract_run<B, R, FLIP8>(w1, a1);
-                                const float2 sz0 = sz[lr0 * p.sz_pitch + grp];
-                                const float2 sz1 = sz[(lr0 + 8) * p.sz_pitch + grp];
+                        for (int i = 0; i < TPW; ++i) {
+                            const int mt = tg + i * ntg;
+                            if (mt >= T)
+                                break;
+                            const int lr0 = mt * 16 + g;
+                            uint32_t w0[(R * B + 31) / 32], w1[(R * B + 31) / 32];
+                            load_run<B, R>(stage, p.pitch, lr0, code0, w0);
+                            load_run<B, R>(stage, p.pitch, lr0 + 8, code0, w1);
+                            uint32_t a0[R / 2], a1[R / 2];
+                            extract_run<B, R, FLIP8>(w0, a0);
+                            extract_run<B, R, FLIP8>(w1, a1);
+                            const int so0 = lr0 * p.sz_pitch + grp, so1 = so0 + 8 * p.sz_pitch;
+                            const float s0 = f16_bits_to_f32(s16[so0]), s1 = f16_bits_to_f32(s16[so1]);
+                            const float zc = static_cast<float>(p.zero_const);
+                            const float zs0 = (p.zeros ? static_cast<float>(z8[so0]) : zc) * s0;
+                            const float zs1 = (p.zeros ? static_cast<float>(z8[so1]) : zc) * s1;
 #pragma unroll
-                                for (int nt = 0; nt < NT; ++nt) {
-                                    // two independent accumulator chains (even / odd j)
-                                    float d[4] = {0.f, 0.f, 0.f, 0.f};
-                                    float d2[4] = {0.f, 0.f, 0.f, 0.f};
+                            for (int nt = 0; nt < NT; ++nt) {
+                                // two independent accumulator chains (even / odd j)
+                                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                                float d2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                                    for (int j = 0; j < R / 4; ++j) {
-                                        uint32_t b0, b1;
-                                        if constexpr (NT <= 2) {
-                                            b0 = bf[j][nt][0];
-                                            b1 = bf[j][nt][1];
-                                        } else {
-                                            const int m = g + 8 * nt;
-                                            uint2 v = make_uint2(0, 0);
-                                            if (m < M)
-                                                v = *reinterpret_cast<const uint2 *>(xb + (j * M + m) * 16);
-                                            b0 = v.x;
-                                            b1 = v.y;
-                                        }
-                                        if (j & 1)
-                                            mma_f16_16816(d2, a0[2 * j], a1[2 * j], a0[2 * j + 1], a1[2 * j + 1], b0, b1);
-                                        else
-                                            mma_f16_16816(d, a0[2 * j], a1[2 * j], a0[2 * j + 1], a1[2 * j + 1], b0, b1);
-                                    }
-#pragma unroll
-                                    for (int e = 0; e < 4; ++e)
-                                        d[e] += d2[e];
-                                    const float2 xv = *reinterpret_cast<const float2 *>(xs + lg * MP + 8 * nt + 2 * t);
-                                    if constexpr (MODE == 0) {
-                                        tot[mt][nt][0] = fmaf(-sz0.y, xv.x, fmaf(sz0.x, d[0], tot[mt][nt][0]));
-                                        tot[mt][nt][1] = fmaf(-sz0.y, xv.y, fmaf(sz0.x, d[1], tot[mt][nt][1]));
-                                        tot[mt][nt][2] = fmaf(-sz1.y, xv.x, fmaf(sz1.x, d[2], tot[mt][nt][2]));
-                                        tot[mt][nt][3] = fmaf(-sz1.y, xv.y, fmaf(sz1.x, d[3], tot[mt][nt][3]));
+                                for (int j = 0; j < R / 4; ++j) {
+                                    uint32_t b0, b1;
+                                    if constexpr (NT <= 2) {
+                                        b0 = bf[j][nt][0];
+                                        b1 = bf[j][nt][1];
                                     } else {
-                                        // exact integers: d and 8 X are below 2^24
-                                        const float acc0 = d[0] - 8.f * xv.x, acc1 = d[1] - 8.f * xv.y;
-                                        const float acc2 = d[2] - 8.f * xv.x, acc3 = d[3] - 8.f * xv.y;
-                                        tot[mt][nt][0] = fmaf(sz0.x, acc0, tot[mt][nt][0]);
-                                        tot[mt][nt][1] = fmaf(sz0.x, acc1, tot[mt][nt][1]);
-                                        tot[mt][nt][2] = fmaf(sz1.x, acc2, tot[mt][nt][2]);
-                                        tot[mt][nt][3] = fmaf(sz1.x, acc3, tot[mt][nt][3]);
-                                        if (p.acc_out) {
-                                            const int tok = 8 * nt + 2 * t;
-                                            const int n0 = row0 + lr0;
-                                            const bool v0 = lr0 < rows_valid, v1 = lr0 + 8 < rows_valid;
-                                            const long long base0 = static_cast<long long>(n0) * ng + grp;
-                                            const long long base1 = static_cast<long long>(n0 + 8) * ng + grp;
-                                            const long long tstride = static_cast<long long>(p.N) * ng;
-                                            if (v0 && tok < M) p.acc_out[tok * tstride + base0] = static_cast<int>(acc0);
-                                            if (v0 && tok + 1 < M) p.acc_out[(tok + 1) * tstride + base0] = static_cast<int>(acc1);
-                                            if (v1 && tok < M) p.acc_out[tok * tstride + base1] = static_cast<int>(acc2);
-                                            if (v1 && tok + 1 < M) p.acc_out[(tok + 1) * tstride + base1] = static_cast<int>(acc3);
-                                        }
+                                        const int m = g + 8 * nt;
+                                        uint2 v = make_uint2(0, 0);
+                                        if (m < M)
+                                            v = *reinterpret_cast<const uint2 *>(xb + (j * M + m) * 16);
+                                        b0 = v.x;
+                                        b1 = v.y;
+                                    }
+                                    if (j & 1)
+                                        mma_f16_16816(d2, a0[2 * j], a1[2 * j], a0[2 * j + 1], a1[2 * j + 1], b0, b1);
+                                    else
+                                        mma_f16_16816(d, a0[2 * j], a1[2 * j], a0[2 * j + 1], a1[2 * j + 1], b0, b1);
+                                }
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    d[e] += d2[e];
+                                if constexpr (MODE == 0) {
+                                    tot[i][nt][0] = fmaf(-zs0, xv[nt].x, fmaf(s0, d[0], tot[i][nt][0]));
+                                    tot[i][nt][1] = fmaf(-zs0, xv[nt].y, fmaf(s0, d[1], tot[i][nt][1]));
+                                    tot[i][nt][2] = fmaf(-zs1, xv[nt].x, fmaf(s1, d[2], tot[i][nt][2]));
+                                    tot[i][nt][3] = fmaf(-zs1, xv[nt].y, fmaf(s1, d[3], tot[i][nt][3]));
+                                } else {
+                                    // exact integers: d and 8 X are below 2^24
+                                    const float acc0 = d[0] - 8.f * xv[nt].x, acc1 = d[1] - 8.f * xv[nt].y;
+                                    const float acc2 = d[2] - 8.f * xv[nt].x, acc3 = d[3] - 8.f * xv[nt].y;
+                                    tot[i][nt][0] = fmaf(s0, acc0, tot[i][nt][0]);
+                                    tot[i][nt][1] = fmaf(s0, acc1, tot[i][nt][1]);
+                                    tot[i][nt][2] = fmaf(s1, acc2, tot[i][nt][2]);
+                                    tot[i][nt][3] = fmaf(s1, acc3, tot[i][nt][3]);
+                                    if (p.acc_out) {
+                                        const int tok = 8 * nt + 2 * t;
+                                        const int n0 = row0 + lr0;
+                                        const bool v0 = lr0 < rows_valid, v1 = lr0 + 8 < rows_valid;
+                                        const long long base0 = static_cast<long long>(n0) * ng + grp;
+                                        const long long base1 = static_cast<long long>(n0 + 8) * ng + grp;
+                                        const long long tstride = static_cast<long long>(p.N) * ng;
+                                        if (v0 && tok < M) p.acc_out[tok * tstride + base0] = static_cast<int>(acc0);
+                                        if (v0 && tok + 1 < M) p.acc_out[(tok + 1) * tstride + base0] = static_cast<int>(acc1);
+                                        if (v1 && tok < M) p.acc_out[tok * tstride + base1] = static_cast<int>(acc2);
+                                        if (v1 && tok + 1 < M) p.acc_out[(tok + 1) * tstride + base1] = static_cast<int>(acc3);
                                     }
                                 }
                             }
@@ -619,33 +577,46 @@ skinny_kernel(const GemvParams p)
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&empty[slot]);
+            // The last warp done with this slot refills it with stage it + ring.
+            if (it + p.ring < total_stages) {
+                __syncwarp();
+                int last = 0;
+                if (lane == 0) {
+                    __threadfence_block();
+                    last = (atomicAdd(&done_count[slot], 1) % kWarps) == kWarps - 1;
+                    __threadfence_block();
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    // the other warps' reads of the slot come before the copy's writes
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    issue_stage(p, it + p.ring, slot, ring, full, r0, nrows, policy);
+                }
+            }
         }
 
         // ---- cross-warp reduction in a fixed order, then the store ----
 #pragma unroll
-        for (int mt = 0; mt < MAXT; ++mt) {
+        for (int i = 0; i < TPW; ++i) {
+            const int mt = tg + i * ntg;
             if (mt < T) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const int row = mt * 16 + g;
                     const int tok = 8 * nt + 2 * t;
-                    *reinterpret_cast<float2 *>(red + (cw * p.rbp + row) * MP + tok) =
-                        make_float2(tot[mt][nt][0], tot[mt][nt][1]);
-                    *reinterpret_cast<float2 *>(red + (cw * p.rbp + row + 8) * MP + tok) =
-                        make_float2(tot[mt][nt][2], tot[mt][nt][3]);
+                    *reinterpret_cast<float2 *>(red + (kid * p.rbp + row) * MP + tok) =
+                        make_float2(tot[i][nt][0], tot[i][nt][1]);
+                    *reinterpret_cast<float2 *>(red + (kid * p.rbp + row + 8) * MP + tok) =
+                        make_float2(tot[i][nt][2], tot[i][nt][3]);
                 }
             }
         }
-        named_sync(1, kCT);
-        for (int idx = ct; idx < M * rows_valid; idx += kCT) {
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < M * rows_valid; idx += kThreads) {
             const int tok = idx / rows_valid;
             const int row = idx - tok * rows_valid;
             float v = 0.f;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w)
+            for (int w = 0; w < ksplit; ++w)
                 v += red[(w * p.rbp + row) * MP + tok];
             if constexpr (MODE == 1)
                 v *= f16_bits_to_f32(p.sa[tok]);
@@ -655,6 +626,16 @@ skinny_kernel(const GemvParams p)
             else
                 reinterpret_cast<uint16_t *>(p.y)[o] = f32_to_f16_bits(v);
         }
+    }
+
+    // After a timed-out wait some copies may not have been waited for: none may
+    // still be landing in shared memory when the CTA exits.
+    __syncthreads();
+    if (!ok && threadIdx.x == 0) {
+        const int first = total_stages > p.ring ? total_stages - p.ring : 0;
+        for (int j = first; j < total_stages; ++j)
+            if (!mbar_wait(&full[j % p.ring], (j / p.ring) & 1, p.status))
+                break;
     }
 }
 

@@ -22,7 +22,7 @@ cudaError_t w4a8_launch(const GemvParams &p, int grid, int smem, cudaStream_t st
 
 qmm_status w4a8_dispatch(const int8_t *xq, const void *sa, const uint8_t *w4, const void *ws,
                          int group, void *y, int32_t *acc_out, int M, int N, int K, int *status,
-                         int num_sms, int smem_optin, cudaStream_t stream)
+                         int num_sms, int smem_optin, int smem_pair, cudaStream_t stream)
 {
     GemvParams p;
     std::memset(&p, 0, sizeof(p));
@@ -43,7 +43,7 @@ qmm_status w4a8_dispatch(const int8_t *xq, const void *sa, const uint8_t *w4, co
     p.ng = K / group;
     p.y_bf16 = 0;
     int grid = 0, smem = 0;
-    qmm_status st = skinny_plan(p, 4, num_sms, smem_optin, &grid, &smem);
+    qmm_status st = skinny_plan(p, 4, num_sms, smem_optin, smem_pair, &grid, &smem);
     if (st != QMM_OK)
         return st;
     p.use_bulk = (reinterpret_cast<uintptr_t>(w4) % 16 == 0) && (p.row_bytes % 16 == 0);

@@ -10,6 +10,6 @@ namespace qmm {
 
 qmm_status w4a8_dispatch(const int8_t *xq, const void *sa, const uint8_t *w4, const void *ws,
                          int group, void *y, int32_t *acc_out, int M, int N, int K, int *status,
-                         int num_sms, int smem_optin, cudaStream_t stream);
+                         int num_sms, int smem_optin, int smem_pair, cudaStream_t stream);
 
 }  // namespace qmm

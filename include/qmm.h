@@ -33,6 +33,17 @@
  *    outputs unspecified and returns; qmm_device_status() reports and clears
  *    it.  Nothing in the library aborts, throws across the ABI or traps.
  *  - Outputs are written with round-to-nearest-even from fp32.
+ *  - Overlap of consecutive calls.  qmm_gemv, qmm_gemm and qmm_w4a8 launch
+ *    with programmatic dependent launch: a call's kernel may start while the
+ *    previous kernel on the stream is still running, and it may read the weight
+ *    arguments (packed / w4, scales / ws, zeros) BEFORE it waits for that
+ *    kernel; activations are read only after the wait.  So the weight
+ *    arguments of a call must not be written by the kernel that directly
+ *    precedes it on the stream if that kernel is itself a qmm_gemv, qmm_gemm
+ *    or qmm_w4a8 call (for example as its y).  Kernels that do not opt in to
+ *    early launch (qmm_pack, and ordinary CUDA / PyTorch kernels) complete
+ *    before the call's kernel starts, so writing the weights with them is
+ *    fine.
  */
 #ifndef QMM_H_
 #define QMM_H_
