@@ -36,7 +36,8 @@ static int plan_layout(GemvParams &p, int rb, int cp, int budget, int max_ring, 
     const int xs_bytes = align_up(cp * ngc * MP * 4, 128);
     const int sz_bytes = align_up(p.rbp * p.sz_pitch * (p.zeros ? 3 : 2), 128);
     const int red_bytes = align_up((1 << p.ksplit_log2) * p.rbp * MP * 4, 128);
-    const int fixed = 128 /* base alignment */ + bar_bytes + x_bytes + xs_bytes + sz_bytes + red_bytes + overrun;
+    // group sums of x and of 2^E x
+    const int fixed = 128 /* base alignment */ + bar_bytes + x_bytes + 2 * xs_bytes + sz_bytes + red_bytes + overrun;
     if (budget - fixed < p.stage_bytes * min_ring)
         return 0;
     int ring = (budget - fixed) / p.stage_bytes;
@@ -49,6 +50,8 @@ static int plan_layout(GemvParams &p, int rb, int cp, int budget, int max_ring, 
     p.off_x = off;
     off += x_bytes;
     p.off_xs = off;
+    off += xs_bytes;
+    p.off_cs = off;
     off += xs_bytes;
     p.off_sz = off;
     off += sz_bytes;

@@ -46,6 +46,8 @@
 
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "gemv.h"
 #include "unpack_plans.h"
@@ -56,17 +58,10 @@ constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kTilesPerWarp = 2;   // 16-row tiles a warp computes per block, at most
 
-// Byte offset of (row, byte) inside a stage: rows sit at a padded pitch.
-__device__ __forceinline__ uint32_t stage_off(int pitch, int row, int byte)
-{
-    return static_cast<uint32_t>(row * pitch + byte);
-}
-
-// The run of R codes starting at code `code0` of a stage row, as NW words
-// shifted so that the run starts at bit 0 of w[0].
+// The run of R codes starting at code `code0` of the stage row at `rowp`, as
+// NW words shifted so that the run starts at bit 0 of w[0].
 template <int B, int R>
-__device__ __forceinline__ void load_run(const uint8_t *stage, int pitch, int row, int code0,
-                                         uint32_t (&w)[(R * B + 31) / 32])
+__device__ __forceinline__ void load_run(const uint8_t *rowp, int code0, uint32_t (&w)[(R * B + 31) / 32])
 {
     constexpr int NW = (R * B + 31) / 32;
     const int bit0 = code0 * B;
@@ -74,28 +69,28 @@ __device__ __forceinline__ void load_run(const uint8_t *stage, int pitch, int ro
         if constexpr (R >= 16) {
 #pragma unroll
             for (int i = 0; i < NW; i += 4) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(stage + stage_off(pitch, row, code0 + 4 * i));
+                const uint4 v = *reinterpret_cast<const uint4 *>(rowp + code0 + 4 * i);
                 w[i] = v.x; w[i + 1] = v.y; w[i + 2] = v.z; w[i + 3] = v.w;
             }
         } else {
-            const uint2 v = *reinterpret_cast<const uint2 *>(stage + stage_off(pitch, row, code0));
+            const uint2 v = *reinterpret_cast<const uint2 *>(rowp + code0);
             w[0] = v.x; w[1] = v.y;
         }
     } else if constexpr ((R * B) % 32 == 0 && B == 4 && NW == 4) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(stage + stage_off(pitch, row, bit0 / 8));
+        const uint4 v = *reinterpret_cast<const uint4 *>(rowp + bit0 / 8);
         w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
     } else if constexpr ((R * B) % 32 == 0) {
         const int wi = bit0 / 32;
         if constexpr (B % 2 == 0 && NW % 2 == 0) {
 #pragma unroll
             for (int i = 0; i < NW; i += 2) {
-                const uint2 v = *reinterpret_cast<const uint2 *>(stage + stage_off(pitch, row, 4 * (wi + i)));
+                const uint2 v = *reinterpret_cast<const uint2 *>(rowp + 4 * (wi + i));
                 w[i] = v.x; w[i + 1] = v.y;
             }
         } else {
 #pragma unroll
             for (int i = 0; i < NW; ++i)
-                w[i] = *reinterpret_cast<const uint32_t *>(stage + stage_off(pitch, row, 4 * (wi + i)));
+                w[i] = *reinterpret_cast<const uint32_t *>(rowp + 4 * (wi + i));
         }
     } else {
         // the run starts inside a word: read NW+1 words and funnel-shift
@@ -104,7 +99,7 @@ __device__ __forceinline__ void load_run(const uint8_t *stage, int pitch, int ro
         uint32_t src[NW + 1];
 #pragma unroll
         for (int i = 0; i <= NW; ++i)
-            src[i] = *reinterpret_cast<const uint32_t *>(stage + stage_off(pitch, row, 4 * (wi + i)));
+            src[i] = *reinterpret_cast<const uint32_t *>(rowp + 4 * (wi + i));
 #pragma unroll
         for (int i = 0; i < NW; ++i)
             w[i] = __funnelshift_r(src[i], src[i + 1], sh);
@@ -141,9 +136,12 @@ __device__ __forceinline__ uint32_t lop3_and_xor(uint32_t a, uint32_t mask, uint
     return d;
 }
 
-// a[i] = fp16 pair (q_lo, q_hi) of plan pair i, exact small integers.  With
-// FLIP8 each 4-bit field is XORed with 8 first (signed int4 -> c xor 8).
-template <int B, int R, bool FLIP8>
+// a[i] = fp16 pair of plan pair i.  With SUB the pair is (q_lo, q_hi), exact
+// small integers; without it (2^E_lo + q_lo, 2^E_hi + q_hi), also exact, and
+// the caller removes sum_k 2^E_k x_k from the dot product instead (one
+// instruction per pair fewer on the integer/half pipe).  With FLIP8 each 4-bit
+// field is XORed with 8 first (signed int4 -> c xor 8).
+template <int B, int R, bool FLIP8, bool SUB>
 __device__ __forceinline__ void extract_run(const uint32_t (&w)[(R * B + 31) / 32],
                                             uint32_t (&a)[R / 2])
 {
@@ -152,7 +150,7 @@ __device__ __forceinline__ void extract_run(const uint32_t (&w)[(R * B + 31) / 3
 #pragma unroll
         for (int i = 0; i < R / 2; ++i) {
             const uint32_t v = prmt(w[i >> 1], 0x64646464u, (i & 1) ? 0x4342u : 0x4140u);
-            a[i] = hsub2(v, 0x64006400u);
+            a[i] = SUB ? hsub2(v, 0x64006400u) : v;
         }
     } else {
         using P = UnpackPlan<B, R>;
@@ -168,8 +166,27 @@ __device__ __forceinline__ void extract_run(const uint32_t (&w)[(R * B + 31) / 3
                                  P::magic(i) | (P::mask(i) & ~(P::mask(i) >> 1)));
             else
                 v = lop3_and_or(win[P::win(i)], P::mask(i), P::magic(i));
-            a[i] = hsub2(v, pow2_half_bits(P::elo(i)) | (pow2_half_bits(P::ehi(i)) << 16));
+            a[i] = SUB ? hsub2(v, pow2_half_bits(P::elo(i)) | (pow2_half_bits(P::ehi(i)) << 16)) : v;
         }
+    }
+}
+
+// The exponent E of code c (0 <= c < R) of a run: without SUB its fp16 value
+// is 2^E + q.
+template <int B, int R>
+__host__ __device__ constexpr int exp_of_code(int c)
+{
+    if constexpr (B == 8) {
+        return 10;   // 0x64 exponent byte: 1024 + code
+    } else {
+        using P = UnpackPlan<B, R>;
+        for (int i = 0; i < R / 2; ++i) {
+            if (P::lo(i) == c)
+                return P::elo(i);
+            if (P::hi(i) == c)
+                return P::ehi(i);
+        }
+        return -100;   // not reached: every code is in a pair
     }
 }
 
@@ -232,12 +249,13 @@ __device__ __forceinline__ void load_act_run(const GemvParams &p, int ch0, int r
 }
 
 // Stages the activations of chunks [ch0, ch0 + nch) in slot order, and the
-// per-group sums X[group][token] (each run summed in k order, the four runs of a
-// group added in order across the quad's lanes: independent of the launch).
+// per-group sums X[group][token]: each run summed pairwise in a fixed order,
+// the four runs of a group added in order across the quad's lanes, so the
+// result does not depend on the launch.
 // MP - M padded tokens get X = 0.
 template <int B, int R, int MODE, int MP>
 __device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t *xp, float *xs,
-                                                  int ch0, int nch)
+                                                  float *cs, int ch0, int nch)
 {
     constexpr int RPC = 128 / R;                 // runs per chunk
     constexpr int NGC = 128 / (4 * R);           // groups per chunk
@@ -251,6 +269,8 @@ __device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t 
         for (int idx = threadIdx.x; idx < ngp * (MP - M); idx += kThreads) {
             const int lg = idx / (MP - M);
             xs[lg * MP + M + (idx - lg * (MP - M))] = 0.f;
+            if (MODE == 0)
+                cs[lg * MP + M + (idx - lg * (MP - M))] = 0.f;
         }
     }
     // warp-uniform trip count: the quad shuffles need every lane
@@ -264,7 +284,7 @@ __device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t 
         for (int u = 0; u < U; ++u) {
             const int idx = wbase + lane + u * kThreads;
             const bool valid = idx < nruns;   // whole quads: nruns is a multiple of 4
-            float sum = 0.f;
+            float sum = 0.f, csum = 0.f;
             int m = 0, lc = 0, gi = 0, tt = 0;
             if (valid) {
                 m = idx / runs_per_tok;
@@ -272,9 +292,31 @@ __device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t 
                 lc = rr / RPC;
                 gi = (rr % RPC) / 4;
                 tt = rr % 4;
+                // pairwise, in a fixed order (exact for int8 inputs)
+                float ps[R];
 #pragma unroll
                 for (int c = 0; c < R; ++c)
-                    sum += f16_bits_to_f32(v[u][c]);   // exact for int8 inputs
+                    ps[c] = f16_bits_to_f32(v[u][c]);
+#pragma unroll
+                for (int w = 1; w < R; w *= 2)
+#pragma unroll
+                    for (int c = 0; c < R; c += 2 * w)
+                        ps[c] += ps[c + w];
+                sum = ps[0];
+                if constexpr (MODE == 0) {
+                    // sum_k 2^E_k x_k: x summed per exponent, then scaled (exact)
+                    // and added in increasing exponent order
+                    float se[11];
+#pragma unroll
+                    for (int e = 0; e < 11; ++e)
+                        se[e] = 0.f;
+#pragma unroll
+                    for (int c = 0; c < R; ++c)
+                        se[exp_of_code<B, R>(c)] += f16_bits_to_f32(v[u][c]);
+#pragma unroll
+                    for (int e = 0; e < 11; ++e)
+                        csum += ldexpf(se[e], e);
+                }
 #pragma unroll
                 for (int j = 0; j < R / 4; ++j) {
                     uint2 o;
@@ -289,6 +331,13 @@ __device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t 
             const float s3 = __shfl_down_sync(0xffffffffu, sum, 3);
             if (valid && tt == 0)
                 xs[(lc * NGC + gi) * MP + m] = ((sum + s1) + s2) + s3;
+            if constexpr (MODE == 0) {
+                const float c1 = __shfl_down_sync(0xffffffffu, csum, 1);
+                const float c2 = __shfl_down_sync(0xffffffffu, csum, 2);
+                const float c3 = __shfl_down_sync(0xffffffffu, csum, 3);
+                if (valid && tt == 0)
+                    cs[(lc * NGC + gi) * MP + m] = ((csum + c1) + c2) + c3;
+            }
         }
     }
 }
@@ -380,7 +429,8 @@ skinny_kernel(const GemvParams p)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
     int *done_count = reinterpret_cast<int *>(full + p.ring);       // warps done per slot (monotonic)
     uint16_t *xp = reinterpret_cast<uint16_t *>(smem + p.off_x);   // [chunk][8][M][4][4]
-    float *xs = reinterpret_cast<float *>(smem + p.off_xs);        // [group][MP]
+    float *xs = reinterpret_cast<float *>(smem + p.off_xs);        // [group][MP] sum x
+    float *cs = reinterpret_cast<float *>(smem + p.off_cs);        // [group][MP] sum 2^E x
     uint16_t *s16 = reinterpret_cast<uint16_t *>(smem + p.off_sz);  // [row][sz_pitch] fp16 scales
     uint8_t *z8 = smem + p.off_sz + p.rbp * p.sz_pitch * 2;          // [row][sz_pitch] zeros
     float *red = reinterpret_cast<float *>(smem + p.off_red);      // [ksplit][rbp][MP]
@@ -420,7 +470,7 @@ skinny_kernel(const GemvParams p)
     // ---- the activations may come from the preceding kernel ----
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (p.nphases == 1)
-        stage_activations<B, R, MODE, MP>(p, xp, xs, 0, p.nchunks);
+        stage_activations<B, R, MODE, MP>(p, xp, xs, cs, 0, p.nchunks);
     __syncthreads();
 
     const int ksplit = 1 << p.ksplit_log2;
@@ -430,6 +480,15 @@ skinny_kernel(const GemvParams p)
     const int g = lane >> 2, t = lane & 3;
     const int M = p.M;
     const int ng = p.ng;
+    const int pitch8 = 8 * p.pitch, sz8 = 8 * p.sz_pitch;
+    const float zc = static_cast<float>(p.zero_const);
+    // activation fragments: token g + 8 nt of 16-code step st sits at xp[st * xstep + xthr + nt * 128]
+    const int xstep = M * 16;
+    const int xthr = g * 16 + t * 4;
+    bool mval[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+        mval[nt] = g + 8 * nt < M;
 
     bool ok = true;
     int it = 0;
@@ -453,13 +512,23 @@ skinny_kernel(const GemvParams p)
                 for (int e = 0; e < 4; ++e)
                     tot[i][nt][e] = 0.f;
 
+        // this warp's tiles (tg, tg + ntg) and their row offsets in a stage and in s16 / z8
+        const int ntl = (tg < T ? 1 : 0) + (tg + ntg < T ? 1 : 0);
+        int roff[TPW], szo[TPW];
+#pragma unroll
+        for (int i = 0; i < TPW; ++i) {
+            const int lr = (tg + i * ntg) * 16 + g;
+            roff[i] = lr * p.pitch;
+            szo[i] = lr * p.sz_pitch;
+        }
+
         int cur_phase = p.nphases == 1 ? 0 : -1;
         for (int s = 0; s < p.stages_per_block; ++s, ++it) {
             const int phase = (s * p.seg_chunks) / p.phase_chunks;
             if (phase != cur_phase) {
                 __syncthreads();   // everyone is done with the previous phase
                 const int ch0 = phase * p.phase_chunks;
-                stage_activations<B, R, MODE, MP>(p, xp, xs, ch0, min(p.phase_chunks, p.nchunks - ch0));
+                stage_activations<B, R, MODE, MP>(p, xp, xs, cs, ch0, min(p.phase_chunks, p.nchunks - ch0));
                 __syncthreads();
                 cur_phase = phase;
             }
@@ -470,60 +539,71 @@ skinny_kernel(const GemvParams p)
                 const uint8_t *stage = ring + static_cast<size_t>(slot) * p.stage_bytes;
                 // this warp's chunks of the stage: cg = kid (mod ksplit)
                 const int cg_first = s * p.seg_chunks + ((kid - s * p.seg_chunks) & (ksplit - 1));
-                const int cg_end = tg < T ? min((s + 1) * p.seg_chunks, p.nchunks) : 0;
+                const int cg_end = min((s + 1) * p.seg_chunks, p.nchunks);
+                // NTL = this warp's tiles in the block (1 or 2), a compile-time count
+                auto run_chunks = [&](auto ntl_c) {
+                    constexpr int NTL = decltype(ntl_c)::value;
 #pragma unroll 1
-                for (int cg = cg_first; cg < cg_end; cg += ksplit) {
-                    const int ci = cg - s * p.seg_chunks;
-                    const int lc = cg - phase * p.phase_chunks;   // chunk within the phase
+                    for (int cg = cg_first; cg < cg_end; cg += ksplit) {
+                        const int ci = cg - s * p.seg_chunks;
+                        const int lc = cg - phase * p.phase_chunks;   // chunk within the phase
 #pragma unroll 1
-                    for (int gi = 0; gi < NGC; ++gi) {
-                        const int grp = cg * NGC + gi;
-                        if (grp >= ng)
-                            break;
-                        const int lg = lc * NGC + gi;
-                        const uint16_t *xb = xp + (static_cast<long long>(lc) * 8 + gi * (R / 4)) * M * 16 + t * 4;
-                        // activation fragments of the R/4 MMAs, shared by the warp's tiles
-                        uint32_t bf[NT <= 2 ? R / 4 : 1][NT <= 2 ? NT : 1][2];
-                        if constexpr (NT <= 2) {
-#pragma unroll
-                            for (int j = 0; j < R / 4; ++j)
-#pragma unroll
-                                for (int nt = 0; nt < NT; ++nt) {
-                                    const int m = g + 8 * nt;
-                                    uint2 v = make_uint2(0, 0);
-                                    if (m < M)
-                                        v = *reinterpret_cast<const uint2 *>(xb + (j * M + m) * 16);
-                                    bf[j][nt][0] = v.x;
-                                    bf[j][nt][1] = v.y;
-                                }
-                        }
-                        float2 xv[NT];
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            xv[nt] = *reinterpret_cast<const float2 *>(xs + lg * MP + 8 * nt + 2 * t);
-                        const int code0 = ci * 128 + gi * 4 * R + t * R;   // within the stage row
-#pragma unroll
-                        for (int i = 0; i < TPW; ++i) {
-                            const int mt = tg + i * ntg;
-                            if (mt >= T)
+                        for (int gi = 0; gi < NGC; ++gi) {
+                            const int grp = cg * NGC + gi;
+                            if (grp >= ng)
                                 break;
-                            const int lr0 = mt * 16 + g;
-                            uint32_t w0[(R * B + 31) / 32], w1[(R * B + 31) / 32];
-                            load_run<B, R>(stage, p.pitch, lr0, code0, w0);
-                            load_run<B, R>(stage, p.pitch, lr0 + 8, code0, w1);
-                            uint32_t a0[R / 2], a1[R / 2];
-                            extract_run<B, R, FLIP8>(w0, a0);
-                            extract_run<B, R, FLIP8>(w1, a1);
-                            const int so0 = lr0 * p.sz_pitch + grp, so1 = so0 + 8 * p.sz_pitch;
-                            const float s0 = f16_bits_to_f32(s16[so0]), s1 = f16_bits_to_f32(s16[so1]);
-                            const float zc = static_cast<float>(p.zero_const);
-                            const float zs0 = (p.zeros ? static_cast<float>(z8[so0]) : zc) * s0;
-                            const float zs1 = (p.zeros ? static_cast<float>(z8[so1]) : zc) * s1;
+                            const int lg = lc * NGC + gi;
+                            const uint16_t *xb = xp + (lc * 8 + gi * (R / 4)) * xstep + xthr;
+                            // activation fragments of the R/4 MMAs, shared by the tiles
+                            uint32_t bf[NT <= 2 ? R / 4 : 1][NT <= 2 ? NT : 1][2];
+                            if constexpr (NT <= 2) {
+#pragma unroll
+                                for (int j = 0; j < R / 4; ++j)
+#pragma unroll
+                                    for (int nt = 0; nt < NT; ++nt) {
+                                        uint2 v = make_uint2(0, 0);
+                                        if (mval[nt])
+                                            v = *reinterpret_cast<const uint2 *>(xb + j * xstep + nt * 128);
+                                        bf[j][nt][0] = v.x;
+                                        bf[j][nt][1] = v.y;
+                                    }
+                            }
+                            float2 xv[NT], cv[NT];
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt) {
-                                // two independent accumulator chains (even / odd j)
-                                float d[4] = {0.f, 0.f, 0.f, 0.f};
-                                float d2[4] = {0.f, 0.f, 0.f, 0.f};
+                                xv[nt] = *reinterpret_cast<const float2 *>(xs + lg * MP + 8 * nt + 2 * t);
+                                if constexpr (MODE == 0)
+                                    cv[nt] = *reinterpret_cast<const float2 *>(cs + lg * MP + 8 * nt + 2 * t);
+                            }
+                            const int code0 = ci * 128 + gi * 4 * R + t * R;   // within the stage row
+                            // raw words and scales of every tile first, so their loads overlap
+                            uint32_t w[NTL][2][(R * B + 31) / 32];
+                            float sc[NTL][2], zs[NTL][2];
+#pragma unroll
+                            for (int i = 0; i < NTL; ++i)
+#pragma unroll
+                                for (int h = 0; h < 2; ++h) {
+                                    load_run<B, R>(stage + roff[i] + h * pitch8, code0, w[i][h]);
+                                    const int so = szo[i] + h * sz8 + grp;
+                                    sc[i][h] = f16_bits_to_f32(s16[so]);
+                                    zs[i][h] = (p.zeros ? static_cast<float>(z8[so]) : zc) * sc[i][h];
+                                }
+                            uint32_t a0[NTL][R / 2], a1[NTL][R / 2];
+#pragma unroll
+                            for (int i = 0; i < NTL; ++i) {
+                                extract_run<B, R, FLIP8, MODE == 1>(w[i][0], a0[i]);
+                                extract_run<B, R, FLIP8, MODE == 1>(w[i][1], a1[i]);
+                            }
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                // per tile two independent accumulator chains (even / odd j),
+                                // the tiles' MMAs interleaved
+                                float d[NTL][2][4];
+#pragma unroll
+                                for (int i = 0; i < NTL; ++i)
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e)
+                                        d[i][0][e] = d[i][1][e] = 0.f;
 #pragma unroll
                                 for (int j = 0; j < R / 4; ++j) {
                                     uint32_t b0, b1;
@@ -531,51 +611,64 @@ skinny_kernel(const GemvParams p)
                                         b0 = bf[j][nt][0];
                                         b1 = bf[j][nt][1];
                                     } else {
-                                        const int m = g + 8 * nt;
                                         uint2 v = make_uint2(0, 0);
-                                        if (m < M)
-                                            v = *reinterpret_cast<const uint2 *>(xb + (j * M + m) * 16);
+                                        if (mval[nt])
+                                            v = *reinterpret_cast<const uint2 *>(xb + j * xstep + nt * 128);
                                         b0 = v.x;
                                         b1 = v.y;
                                     }
-                                    if (j & 1)
-                                        mma_f16_16816(d2, a0[2 * j], a1[2 * j], a0[2 * j + 1], a1[2 * j + 1], b0, b1);
-                                    else
-                                        mma_f16_16816(d, a0[2 * j], a1[2 * j], a0[2 * j + 1], a1[2 * j + 1], b0, b1);
+#pragma unroll
+                                    for (int i = 0; i < NTL; ++i)
+                                        mma_f16_16816(d[i][j & 1], a0[i][2 * j], a1[i][2 * j], a0[i][2 * j + 1],
+                                                      a1[i][2 * j + 1], b0, b1);
                                 }
 #pragma unroll
-                                for (int e = 0; e < 4; ++e)
-                                    d[e] += d2[e];
-                                if constexpr (MODE == 0) {
-                                    tot[i][nt][0] = fmaf(-zs0, xv[nt].x, fmaf(s0, d[0], tot[i][nt][0]));
-                                    tot[i][nt][1] = fmaf(-zs0, xv[nt].y, fmaf(s0, d[1], tot[i][nt][1]));
-                                    tot[i][nt][2] = fmaf(-zs1, xv[nt].x, fmaf(s1, d[2], tot[i][nt][2]));
-                                    tot[i][nt][3] = fmaf(-zs1, xv[nt].y, fmaf(s1, d[3], tot[i][nt][3]));
-                                } else {
-                                    // exact integers: d and 8 X are below 2^24
-                                    const float acc0 = d[0] - 8.f * xv[nt].x, acc1 = d[1] - 8.f * xv[nt].y;
-                                    const float acc2 = d[2] - 8.f * xv[nt].x, acc3 = d[3] - 8.f * xv[nt].y;
-                                    tot[i][nt][0] = fmaf(s0, acc0, tot[i][nt][0]);
-                                    tot[i][nt][1] = fmaf(s0, acc1, tot[i][nt][1]);
-                                    tot[i][nt][2] = fmaf(s1, acc2, tot[i][nt][2]);
-                                    tot[i][nt][3] = fmaf(s1, acc3, tot[i][nt][3]);
-                                    if (p.acc_out) {
-                                        const int tok = 8 * nt + 2 * t;
-                                        const int n0 = row0 + lr0;
-                                        const bool v0 = lr0 < rows_valid, v1 = lr0 + 8 < rows_valid;
-                                        const long long base0 = static_cast<long long>(n0) * ng + grp;
-                                        const long long base1 = static_cast<long long>(n0 + 8) * ng + grp;
-                                        const long long tstride = static_cast<long long>(p.N) * ng;
-                                        if (v0 && tok < M) p.acc_out[tok * tstride + base0] = static_cast<int>(acc0);
-                                        if (v0 && tok + 1 < M) p.acc_out[(tok + 1) * tstride + base0] = static_cast<int>(acc1);
-                                        if (v1 && tok < M) p.acc_out[tok * tstride + base1] = static_cast<int>(acc2);
-                                        if (v1 && tok + 1 < M) p.acc_out[(tok + 1) * tstride + base1] = static_cast<int>(acc3);
+                                for (int i = 0; i < NTL; ++i) {
+                                    float dd[4];
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e)
+                                        dd[e] = d[i][0][e] + d[i][1][e];
+                                    if constexpr (MODE == 0) {
+                                        // the products carried 2^E x as well
+                                        dd[0] -= cv[nt].x;
+                                        dd[1] -= cv[nt].y;
+                                        dd[2] -= cv[nt].x;
+                                        dd[3] -= cv[nt].y;
+                                        tot[i][nt][0] = fmaf(-zs[i][0], xv[nt].x, fmaf(sc[i][0], dd[0], tot[i][nt][0]));
+                                        tot[i][nt][1] = fmaf(-zs[i][0], xv[nt].y, fmaf(sc[i][0], dd[1], tot[i][nt][1]));
+                                        tot[i][nt][2] = fmaf(-zs[i][1], xv[nt].x, fmaf(sc[i][1], dd[2], tot[i][nt][2]));
+                                        tot[i][nt][3] = fmaf(-zs[i][1], xv[nt].y, fmaf(sc[i][1], dd[3], tot[i][nt][3]));
+                                    } else {
+                                        // exact integers: d and 8 X are below 2^24
+                                        const float acc0 = dd[0] - 8.f * xv[nt].x, acc1 = dd[1] - 8.f * xv[nt].y;
+                                        const float acc2 = dd[2] - 8.f * xv[nt].x, acc3 = dd[3] - 8.f * xv[nt].y;
+                                        tot[i][nt][0] = fmaf(sc[i][0], acc0, tot[i][nt][0]);
+                                        tot[i][nt][1] = fmaf(sc[i][0], acc1, tot[i][nt][1]);
+                                        tot[i][nt][2] = fmaf(sc[i][1], acc2, tot[i][nt][2]);
+                                        tot[i][nt][3] = fmaf(sc[i][1], acc3, tot[i][nt][3]);
+                                        if (p.acc_out) {
+                                            const int lr0 = (tg + i * ntg) * 16 + g;
+                                            const int tok = 8 * nt + 2 * t;
+                                            const int n0 = row0 + lr0;
+                                            const bool v0 = lr0 < rows_valid, v1 = lr0 + 8 < rows_valid;
+                                            const long long base0 = static_cast<long long>(n0) * ng + grp;
+                                            const long long base1 = static_cast<long long>(n0 + 8) * ng + grp;
+                                            const long long tstride = static_cast<long long>(p.N) * ng;
+                                            if (v0 && tok < M) p.acc_out[tok * tstride + base0] = static_cast<int>(acc0);
+                                            if (v0 && tok + 1 < M) p.acc_out[(tok + 1) * tstride + base0] = static_cast<int>(acc1);
+                                            if (v1 && tok < M) p.acc_out[tok * tstride + base1] = static_cast<int>(acc2);
+                                            if (v1 && tok + 1 < M) p.acc_out[(tok + 1) * tstride + base1] = static_cast<int>(acc3);
+                                        }
                                     }
                                 }
                             }
                         }
                     }
-                }
+                };
+                if (ntl == 2)
+                    run_chunks(std::integral_constant<int, 2>{});
+                else if (ntl == 1)
+                    run_chunks(std::integral_constant<int, 1>{});
             }
             // The last warp done with this slot refills it with stage it + ring.
             if (it + p.ring < total_stages) {
