@@ -45,7 +45,7 @@ WORKLOAD = ("decode GEMV width sweep: M=1, K=N=4096, bits 1..8, group 128, "
             "z=2^(b-1), fp16 activations/outputs, fp32 accumulation")
 BITS = list(range(1, 9))
 PROFILE = os.path.join(ROOT, "profiles", "qmm_gemv_decode_sweep.txt")
-KERNEL_SOURCES = ["gemv.cu", "common.cuh", "unpack_plans.h"]
+KERNEL_SOURCES = ["skinny.cuh", "gemv.cu", "gemv.h", "common.cuh", "unpack_plans.h"]
 
 
 def kernel_source_digest() -> str:
@@ -539,7 +539,7 @@ def run_ours(args, world, rank, local):
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_kind": peak_kind,
-                         "traffic": traffic, "kernel": "qmm::gemv_kernel (all widths)",
+                         "traffic": traffic, "kernel": "qmm::skinny_kernel<b,1,32,0> (b = 1..8)",
                          "algorithmic_bytes_per_launch": round(step_bytes / len(probs)),
                          "frac_of_8TBs": round(achieved / 8000.0, 4),
                          "duration_source": how},

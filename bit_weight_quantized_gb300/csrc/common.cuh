@@ -64,21 +64,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// try_wait that lets the thread sleep for up to `ns` nanoseconds (it is woken
-// when the phase completes), so that waiting warps do not take issue slots.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-
 // Waits for the phase with the given parity to complete.  Returns false (and
 // records QMM_ERR_TIMEOUT) if it has not completed within kWaitCycles.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *status)
@@ -86,7 +71,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *s
     if (mbar_try_wait(bar, parity))
         return true;
     long long start = clock64();
-    while (!mbar_try_wait_sleep(bar, parity, 100000)) {
+    while (!mbar_try_wait(bar, parity)) {
         if (clock64() - start > kWaitCycles) {
             record_error(status, QMM_ERR_TIMEOUT);
             return false;
