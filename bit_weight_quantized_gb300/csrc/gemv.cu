@@ -26,15 +26,15 @@ static int plan_layout(GemvParams &p, int rb, int cp, int budget, int max_ring, 
     p.rbp = align_up(rb, 16);
     p.phase_chunks = cp;
     p.nphases = (p.nchunks + cp - 1) / cp;
-    // a slot holds rb rows; the MMA tiles also read the rows up to rbp, whose
-    // results are dropped: those reads land in the slack at the end
+    // a slot holds rb rows (tile rows past rb read row rb - 1); a run that starts
+    // inside a word reads one word past its end: 16 bytes of slack after the ring
     p.stage_bytes = align_up(rb * p.pitch, 128);
-    const int overrun = align_up((p.rbp - rb) * p.pitch + 16, 128);
+    const int overrun = 128;
     p.sz_pitch = p.ng + ((p.ng & 1) ? 0 : 1);   // odd: the eight rows of a tile hit different banks
     const int bar_bytes = align_up(kMaxRing * 12, 128);
     const int x_bytes = align_up(p.M * cp * 128 * 2, 128);
     const int xs_bytes = align_up(cp * ngc * MP * 4, 128);
-    const int sz_bytes = align_up(p.rbp * p.sz_pitch * (p.zeros ? 3 : 2), 128);
+    const int sz_bytes = align_up(p.rbp * p.sz_pitch * 8, 128);   // float2 (s, z*s)
     const int red_bytes = align_up((1 << p.ksplit_log2) * p.rbp * MP * 4, 128);
     // group sums of x and of 2^E x
     const int fixed = 128 /* base alignment */ + bar_bytes + x_bytes + 2 * xs_bytes + sz_bytes + red_bytes + overrun;
@@ -97,29 +97,52 @@ qmm_status skinny_plan(GemvParams &p, int bits, int num_sms, int smem_max, int s
     if (seg0 > p.nchunks)
         seg0 = p.nchunks;
     const int budgets[2] = {smem_pair, smem_max};
-    // Preference: a layout that lets two CTAs share an SM (if it needs no more
-    // phases or blocks than the smallest); then one activation phase; fewer row blocks (a block switch drains the pipeline); then the
-    // most bytes in flight, with longer segments unless a shorter one keeps at
-    // least 15% more in flight.  Segments under kMinSegBytes come last.
+    // Candidates are ranked by: how often the activations are staged (once with
+    // one phase or one block, else once per block), row blocks (a block switch
+    // drains the pipeline), phases, then bytes in flight (a shorter segment only
+    // for at least 15% more), then segment length.  Segments under
+    // kMinSegBytes are tried only when nothing else fits.  A layout that lets
+    // two CTAs share an SM is taken first, if it needs one phase, the fewest
+    // blocks and no short segments.
+    struct Cand {
+        int nph, nblk, seg, kl;
+        long long inflight;
+    };
+    auto better = [](const Cand &a, const Cand &b) {   // a ranks before b
+        const int ra = (a.nph == 1 || a.nblk == 1) ? 1 : a.nblk;
+        const int rb_ = (b.nph == 1 || b.nblk == 1) ? 1 : b.nblk;
+        if (ra != rb_)
+            return ra < rb_;
+        if (a.nblk != b.nblk)
+            return a.nblk < b.nblk;
+        if (a.nph != b.nph)
+            return a.nph < b.nph;
+        if (a.inflight * 100 > b.inflight * 115)
+            return true;
+        if (b.inflight * 100 > a.inflight * 115)
+            return false;
+        return a.seg > b.seg;
+    };
     for (int bi = 0; bi < 2; ++bi) {
         const int budget = budgets[bi];
         if (budget <= 0 || budget > smem_max)
             continue;
-        // sharing an SM is taken only without extra phases, row blocks or short segments
         const int nph_max = bi == 0 ? 1 : p.nchunks;
-        const int nblk_max = bi == 0 ? nblk0 : nblk0 + 4;
+        const int nblk_max = bi == 0 ? nblk0 : nblk0 + 8;
         for (int pass = 0; pass < (bi == 0 ? 1 : 2); ++pass) {
+            bool found = false;
+            Cand best = {0, 0, 0, 0, 0};
             for (int nph = 1; nph <= nph_max; ++nph) {
                 for (int nblk = nblk0; nblk <= nblk_max; ++nblk) {
                     const int rb = (rows_max + nblk - 1) / nblk;
+                    if (rb < 1)
+                        break;
                     // the largest K split whose tile groups cover the tiles, two per warp
                     const int tiles = (rb + 15) / 16;
                     int kl = 3;
                     while (kl > 0 && tiles > kTilesPerWarp * (kWarps >> kl))
                         --kl;
                     p.ksplit_log2 = kl;
-                    int best_seg = 0;
-                    long long best_inflight = 0;
                     for (int seg = seg0; seg >= 1; --seg) {
                         if (pass == 0 && seg < seg0 && seg * 16 * bits < kMinSegBytes)
                             break;
@@ -137,22 +160,24 @@ qmm_status skinny_plan(GemvParams &p, int bits, int num_sms, int smem_max, int s
                         if (inflight > p.row_bytes * nblk)
                             inflight = p.row_bytes * nblk;
                         inflight *= rb;
-                        if (best_seg == 0 || inflight * 100 > best_inflight * 115) {
-                            best_seg = seg;
-                            best_inflight = inflight;
+                        const Cand c = {nph, nblk, seg, kl, inflight};
+                        if (!found || better(c, best)) {
+                            best = c;
+                            found = true;
                         }
                     }
-                    if (best_seg) {
-                        set_segment(p, bits, best_seg);
-                        const int cp = ((p.stages_per_block + nph - 1) / nph) * best_seg;
-                        const int total = nblk * p.stages_per_block;
-                        const int max_ring = total < kMaxRing ? total : kMaxRing;
-                        const int smem = plan_layout(p, rb, cp, budget, max_ring, max_ring < 2 ? max_ring : 2);
-                        *grid_out = grid;
-                        *smem_out = smem;
-                        return QMM_OK;
-                    }
                 }
+            }
+            if (found) {
+                const int rb = (rows_max + best.nblk - 1) / best.nblk;
+                p.ksplit_log2 = best.kl;
+                set_segment(p, bits, best.seg);
+                const int cp = ((p.stages_per_block + best.nph - 1) / best.nph) * best.seg;
+                const int total = best.nblk * p.stages_per_block;
+                const int max_ring = total < kMaxRing ? total : kMaxRing;
+                *smem_out = plan_layout(p, rb, cp, budget, max_ring, max_ring < 2 ? max_ring : 2);
+                *grid_out = grid;
+                return QMM_OK;
             }
         }
     }

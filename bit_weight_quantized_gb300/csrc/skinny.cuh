@@ -317,13 +317,16 @@ __device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t 
                     for (int e = 0; e < 11; ++e)
                         csum += ldexpf(se[e], e);
                 }
+                // the run's R slots, contiguous: [chunk][group][token][quad thread][R]
+                uint16_t *dst = xp + ((static_cast<long long>(lc * NGC + gi) * M + m) * 4 + tt) * R;
 #pragma unroll
-                for (int j = 0; j < R / 4; ++j) {
-                    uint2 o;
+                for (int j = 0; j < R / 4; j += 2) {
+                    uint4 o;
                     o.x = v[u][code_of_slot<B, R>(4 * j + 0)] | (static_cast<uint32_t>(v[u][code_of_slot<B, R>(4 * j + 1)]) << 16);
                     o.y = v[u][code_of_slot<B, R>(4 * j + 2)] | (static_cast<uint32_t>(v[u][code_of_slot<B, R>(4 * j + 3)]) << 16);
-                    const int jj = gi * (R / 4) + j;
-                    *reinterpret_cast<uint2 *>(xp + ((static_cast<long long>(lc) * 8 + jj) * M + m) * 16 + tt * 4) = o;
+                    o.z = v[u][code_of_slot<B, R>(4 * j + 4)] | (static_cast<uint32_t>(v[u][code_of_slot<B, R>(4 * j + 5)]) << 16);
+                    o.w = v[u][code_of_slot<B, R>(4 * j + 6)] | (static_cast<uint32_t>(v[u][code_of_slot<B, R>(4 * j + 7)]) << 16);
+                    *reinterpret_cast<uint4 *>(dst + 4 * j) = o;
                 }
             }
             const float s1 = __shfl_down_sync(0xffffffffu, sum, 1);
@@ -342,10 +345,9 @@ __device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t 
     }
 }
 
-// Scales (fp16 bits, as stored) and per-group zeros (uint8) of a block's rows,
-// eight loads per thread in flight; the fold converts them (exactly) at use.
-__device__ __forceinline__ void stage_scales(const GemvParams &p, uint16_t *s16, uint8_t *z8, int row0,
-                                             int rows_valid)
+// Scales and zero*scale of a block's rows as float2 (s, z*s), eight loads per
+// thread in flight.
+__device__ __forceinline__ void stage_scales(const GemvParams &p, float2 *sz, int row0, int rows_valid)
 {
     const int ng = p.ng;
     const int n = rows_valid * ng;
@@ -356,7 +358,7 @@ __device__ __forceinline__ void stage_scales(const GemvParams &p, uint16_t *s16,
         for (int u = 0; u < 8; ++u) {
             const int idx = base + u * kThreads;
             sv[u] = 0;
-            zv[u] = 0;
+            zv[u] = static_cast<uint8_t>(p.zero_const);
             if (idx < n) {
                 const long long off = static_cast<long long>(row0) * ng + idx;
                 sv[u] = p.scales[off];
@@ -369,10 +371,8 @@ __device__ __forceinline__ void stage_scales(const GemvParams &p, uint16_t *s16,
             const int idx = base + u * kThreads;
             if (idx < n) {
                 const int rr = idx / ng;
-                const int o = rr * p.sz_pitch + (idx - rr * ng);
-                s16[o] = sv[u];
-                if (p.zeros)
-                    z8[o] = zv[u];
+                const float sf = f16_bits_to_f32(sv[u]);
+                sz[rr * p.sz_pitch + (idx - rr * ng)] = make_float2(sf, static_cast<float>(zv[u]) * sf);
             }
         }
     }
@@ -428,11 +428,10 @@ skinny_kernel(const GemvParams p)
                                                 ~static_cast<uintptr_t>(127));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
     int *done_count = reinterpret_cast<int *>(full + p.ring);       // warps done per slot (monotonic)
-    uint16_t *xp = reinterpret_cast<uint16_t *>(smem + p.off_x);   // [chunk][8][M][4][4]
+    uint16_t *xp = reinterpret_cast<uint16_t *>(smem + p.off_x);   // [chunk][group][M][4][R]
     float *xs = reinterpret_cast<float *>(smem + p.off_xs);        // [group][MP] sum x
     float *cs = reinterpret_cast<float *>(smem + p.off_cs);        // [group][MP] sum 2^E x
-    uint16_t *s16 = reinterpret_cast<uint16_t *>(smem + p.off_sz);  // [row][sz_pitch] fp16 scales
-    uint8_t *z8 = smem + p.off_sz + p.rbp * p.sz_pitch * 2;          // [row][sz_pitch] zeros
+    float2 *sz = reinterpret_cast<float2 *>(smem + p.off_sz);       // [row][sz_pitch] (s, z*s)
     float *red = reinterpret_cast<float *>(smem + p.off_red);      // [ksplit][rbp][MP]
     uint8_t *ring = smem + p.off_ring;
 
@@ -465,7 +464,7 @@ skinny_kernel(const GemvParams p)
         for (int it = 0; it < first; ++it)
             issue_stage(p, it, it, ring, full, r0, nrows, policy);
     }
-    stage_scales(p, s16, z8, r0, min(p.rb, nrows));
+    stage_scales(p, sz, r0, min(p.rb, nrows));
 
     // ---- the activations may come from the preceding kernel ----
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -480,15 +479,14 @@ skinny_kernel(const GemvParams p)
     const int g = lane >> 2, t = lane & 3;
     const int M = p.M;
     const int ng = p.ng;
-    const int pitch8 = 8 * p.pitch, sz8 = 8 * p.sz_pitch;
-    const float zc = static_cast<float>(p.zero_const);
-    // activation fragments: token g + 8 nt of 16-code step st sits at xp[st * xstep + xthr + nt * 128]
-    const int xstep = M * 16;
-    const int xthr = g * 16 + t * 4;
-    bool mval[NT];
+    // activation fragments of token g + 8 nt and quad thread t: R contiguous slots at
+    // xp[(chunk * NGC + group) * M * 4 R + xlane[nt]]; tokens past M read token M - 1
+    // (their accumulator columns are never stored)
+    const int gstride = M * 4 * R;
+    int xlane[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
-        mval[nt] = g + 8 * nt < M;
+        xlane[nt] = (min(g + 8 * nt, M - 1) * 4 + t) * R;
 
     bool ok = true;
     int it = 0;
@@ -498,8 +496,8 @@ skinny_kernel(const GemvParams p)
         const int T = (rows_valid + 15) / 16;
 
         if (blk > 0) {
-            __syncthreads();   // the previous block's epilogue is done with s16 / z8 / red
-            stage_scales(p, s16, z8, row0, rows_valid);
+            __syncthreads();   // the previous block's epilogue is done with sz / red
+            stage_scales(p, sz, row0, rows_valid);
             __syncthreads();
         }
 
@@ -512,15 +510,18 @@ skinny_kernel(const GemvParams p)
                 for (int e = 0; e < 4; ++e)
                     tot[i][nt][e] = 0.f;
 
-        // this warp's tiles (tg, tg + ntg) and their row offsets in a stage and in s16 / z8
+        // this warp's tiles (tg, tg + ntg) and their row offsets in a stage and in sz
         const int ntl = (tg < T ? 1 : 0) + (tg + ntg < T ? 1 : 0);
-        int roff[TPW], szo[TPW];
+        // rows past the block's end read row rb - 1 (in the slot); their results are dropped
+        int roff[TPW][2], szo[TPW][2];
 #pragma unroll
-        for (int i = 0; i < TPW; ++i) {
-            const int lr = (tg + i * ntg) * 16 + g;
-            roff[i] = lr * p.pitch;
-            szo[i] = lr * p.sz_pitch;
-        }
+        for (int i = 0; i < TPW; ++i)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int lr = min((tg + i * ntg) * 16 + g + 8 * h, p.rb - 1);
+                roff[i][h] = lr * p.pitch;
+                szo[i][h] = lr * p.sz_pitch;
+            }
 
         int cur_phase = p.nphases == 1 ? 0 : -1;
         for (int s = 0; s < p.stages_per_block; ++s, ++it) {
@@ -553,19 +554,19 @@ skinny_kernel(const GemvParams p)
                             if (grp >= ng)
                                 break;
                             const int lg = lc * NGC + gi;
-                            const uint16_t *xb = xp + (lc * 8 + gi * (R / 4)) * xstep + xthr;
+                            const uint16_t *xg = xp + (lc * NGC + gi) * gstride;
                             // activation fragments of the R/4 MMAs, shared by the tiles
                             uint32_t bf[NT <= 2 ? R / 4 : 1][NT <= 2 ? NT : 1][2];
                             if constexpr (NT <= 2) {
 #pragma unroll
-                                for (int j = 0; j < R / 4; ++j)
+                                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                                    for (int nt = 0; nt < NT; ++nt) {
-                                        uint2 v = make_uint2(0, 0);
-                                        if (mval[nt])
-                                            v = *reinterpret_cast<const uint2 *>(xb + j * xstep + nt * 128);
+                                    for (int j = 0; j < R / 4; j += 2) {
+                                        const uint4 v = *reinterpret_cast<const uint4 *>(xg + xlane[nt] + 4 * j);
                                         bf[j][nt][0] = v.x;
                                         bf[j][nt][1] = v.y;
+                                        bf[j + 1][nt][0] = v.z;
+                                        bf[j + 1][nt][1] = v.w;
                                     }
                             }
                             float2 xv[NT], cv[NT];
@@ -583,10 +584,10 @@ skinny_kernel(const GemvParams p)
                             for (int i = 0; i < NTL; ++i)
 #pragma unroll
                                 for (int h = 0; h < 2; ++h) {
-                                    load_run<B, R>(stage + roff[i] + h * pitch8, code0, w[i][h]);
-                                    const int so = szo[i] + h * sz8 + grp;
-                                    sc[i][h] = f16_bits_to_f32(s16[so]);
-                                    zs[i][h] = (p.zeros ? static_cast<float>(z8[so]) : zc) * sc[i][h];
+                                    load_run<B, R>(stage + roff[i][h], code0, w[i][h]);
+                                    const float2 v = sz[szo[i][h] + grp];
+                                    sc[i][h] = v.x;
+                                    zs[i][h] = v.y;
                                 }
                             uint32_t a0[NTL][R / 2], a1[NTL][R / 2];
 #pragma unroll
@@ -611,9 +612,7 @@ skinny_kernel(const GemvParams p)
                                         b0 = bf[j][nt][0];
                                         b1 = bf[j][nt][1];
                                     } else {
-                                        uint2 v = make_uint2(0, 0);
-                                        if (mval[nt])
-                                            v = *reinterpret_cast<const uint2 *>(xb + j * xstep + nt * 128);
+                                        const uint2 v = *reinterpret_cast<const uint2 *>(xg + xlane[nt] + 4 * j);
                                         b0 = v.x;
                                         b1 = v.y;
                                     }
