@@ -345,34 +345,35 @@ __device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t 
     }
 }
 
-// Scales and zero*scale of a block's rows as float2 (s, z*s), eight loads per
-// thread in flight.
-__device__ __forceinline__ void stage_scales(const GemvParams &p, float2 *sz, int row0, int rows_valid)
+// Scales and zero*scale of a block's rows as float2 (s, z*s): warp w takes rows
+// w, w + 8, ..., four rows' loads in flight per lane.
+static __device__ __noinline__ void stage_scales(const GemvParams &p, float2 *sz, int row0, int rows_valid)
 {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ng = p.ng;
-    const int n = rows_valid * ng;
-    for (int base = threadIdx.x; base < n; base += 8 * kThreads) {
-        uint16_t sv[8];
-        uint8_t zv[8];
+    for (int r = warp; r < rows_valid; r += 4 * kWarps) {
+        for (int g = lane; g < ng; g += 32) {
+            uint16_t sv[4];
+            uint8_t zv[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int idx = base + u * kThreads;
-            sv[u] = 0;
-            zv[u] = static_cast<uint8_t>(p.zero_const);
-            if (idx < n) {
-                const long long off = static_cast<long long>(row0) * ng + idx;
-                sv[u] = p.scales[off];
-                if (p.zeros)
-                    zv[u] = p.zeros[off];
+            for (int u = 0; u < 4; ++u) {
+                const int rr = r + u * kWarps;
+                sv[u] = 0;
+                zv[u] = static_cast<uint8_t>(p.zero_const);
+                if (rr < rows_valid) {
+                    const long long off = static_cast<long long>(row0 + rr) * ng + g;
+                    sv[u] = p.scales[off];
+                    if (p.zeros)
+                        zv[u] = p.zeros[off];
+                }
             }
-        }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int idx = base + u * kThreads;
-            if (idx < n) {
-                const int rr = idx / ng;
-                const float sf = f16_bits_to_f32(sv[u]);
-                sz[rr * p.sz_pitch + (idx - rr * ng)] = make_float2(sf, static_cast<float>(zv[u]) * sf);
+            for (int u = 0; u < 4; ++u) {
+                const int rr = r + u * kWarps;
+                if (rr < rows_valid) {
+                    const float sf = f16_bits_to_f32(sv[u]);
+                    sz[rr * p.sz_pitch + g] = make_float2(sf, static_cast<float>(zv[u]) * sf);
+                }
             }
         }
     }
@@ -381,7 +382,7 @@ __device__ __forceinline__ void stage_scales(const GemvParams &p, float2 *sz, in
 // Issues pipeline stage `it` (K segment s of row block blk) into ring slot
 // `slot`: one bulk copy per row, completing on full[slot].  Called by a whole
 // warp.  Without 16-byte aligned rows the warp copies with 4-byte loads.
-__device__ __forceinline__ void issue_stage(const GemvParams &p, int it, int slot, uint8_t *ring,
+static __device__ __noinline__ void issue_stage(const GemvParams &p, int it, int slot, uint8_t *ring,
                                             uint64_t *full, int r0, int nrows, uint64_t policy)
 {
     const int lane = threadIdx.x & 31;
@@ -468,9 +469,6 @@ skinny_kernel(const GemvParams p)
 
     // ---- the activations may come from the preceding kernel ----
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (p.nphases == 1)
-        stage_activations<B, R, MODE, MP>(p, xp, xs, cs, 0, p.nchunks);
-    __syncthreads();
 
     const int ksplit = 1 << p.ksplit_log2;
     const int kid = warp & (ksplit - 1);          // K split: chunks = kid (mod ksplit)
@@ -489,7 +487,9 @@ skinny_kernel(const GemvParams p)
         xlane[nt] = (min(g + 8 * nt, M - 1) * 4 + t) * R;
 
     bool ok = true;
-    int it = 0;
+    int it = 0;                 // pipeline stage, and its slot and phase parity
+    int slot = 0;
+    uint32_t parity = 0;
     for (int blk = 0; blk < nblocks; ++blk) {
         const int row0 = r0 + blk * p.rb;
         const int rows_valid = min(p.rb, r0 + nrows - row0);
@@ -523,9 +523,15 @@ skinny_kernel(const GemvParams p)
                 szo[i][h] = lr * p.sz_pitch;
             }
 
-        int cur_phase = p.nphases == 1 ? 0 : -1;
+        // activations: staged at the first stage of block 0, or per phase of every
+        // block when they are staged in K phases
+        int cur_phase = (p.nphases == 1 && blk > 0) ? 0 : -1;
+        int phase = 0, phase_end = p.phase_chunks;
         for (int s = 0; s < p.stages_per_block; ++s, ++it) {
-            const int phase = (s * p.seg_chunks) / p.phase_chunks;
+            while (s * p.seg_chunks >= phase_end) {
+                ++phase;
+                phase_end += p.phase_chunks;
+            }
             if (phase != cur_phase) {
                 __syncthreads();   // everyone is done with the previous phase
                 const int ch0 = phase * p.phase_chunks;
@@ -533,9 +539,8 @@ skinny_kernel(const GemvParams p)
                 __syncthreads();
                 cur_phase = phase;
             }
-            const int slot = it % p.ring;
             if (ok)
-                ok = mbar_wait(&full[slot], (it / p.ring) & 1, p.status);
+                ok = mbar_wait(&full[slot], parity, p.status);
             if (ok) {
                 const uint8_t *stage = ring + static_cast<size_t>(slot) * p.stage_bytes;
                 // this warp's chunks of the stage: cg = kid (mod ksplit)
@@ -685,6 +690,10 @@ skinny_kernel(const GemvParams p)
                     issue_stage(p, it + p.ring, slot, ring, full, r0, nrows, policy);
                 }
             }
+            if (++slot == p.ring) {
+                slot = 0;
+                parity ^= 1u;
+            }
         }
 
         // ---- cross-warp reduction in a fixed order, then the store ----
@@ -704,9 +713,11 @@ skinny_kernel(const GemvParams p)
             }
         }
         __syncthreads();
-        for (int idx = threadIdx.x; idx < M * rows_valid; idx += kThreads) {
-            const int tok = idx / rows_valid;
-            const int row = idx - tok * rows_valid;
+        for (int idx = threadIdx.x; idx < rows_valid * MP; idx += kThreads) {
+            const int tok = idx & (MP - 1);
+            const int row = idx / MP;   // MP is a power of two
+            if (tok >= M)
+                continue;
             float v = 0.f;
             for (int w = 0; w < ksplit; ++w)
                 v += red[(w * p.rbp + row) * MP + tok];
