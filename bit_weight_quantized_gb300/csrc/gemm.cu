@@ -33,7 +33,7 @@ constexpr int kWK = 256;           // codes per packed-weight stage (128 bytes p
 constexpr int kKPerW = kWK / kBK;  // K steps per packed-weight stage
 constexpr int kXStages = 3;
 constexpr int kWStages = 2;
-constexpr int kBStages = 2;
+constexpr int kBStages = 3;
 constexpr int kMTiles = 2;         // accumulators per pass
 constexpr int kAccCols = 256;      // TMEM column stride between the accumulators
 constexpr int kTmemCols = 512;
