@@ -41,8 +41,10 @@ constexpr int kTmemCols = 512;
 constexpr int kEpiWarps = 4;       // warps 0..3: epilogue, TMEM lane quarter = warp id
 constexpr int kProdWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kDeqWarp0 = 6;       // warps 6..11: dequant, one thread per tile column
-constexpr int kDeqWarps = kBN / 32;
+constexpr int kDeqWarp0 = 6;       // warps 6..: dequant, kDeqPerCol threads per tile column
+constexpr int kDeqPerCol = 2;      // each takes 64 / kDeqPerCol codes of every 64
+constexpr int kDeqWords = 8 / kDeqPerCol;
+constexpr int kDeqWarps = kDeqPerCol * kBN / 32;
 constexpr int kThreads = 32 * (kDeqWarp0 + kDeqWarps);
 
 constexpr int kXTileBytes = kBM * kBK * 2;     // 16 KB
@@ -194,28 +196,26 @@ struct GroupConst {
     uint32_t off2;
 };
 
-// raw scale / zero of the groups a packed-weight stage touches: entry [j][h]
-// covers codes 64j + 32h .. +31 of the stage
+// raw scale / zero of the groups of one half (32 codes of every 64) of a
+// packed-weight stage: entry [j] covers codes 64j + 32h .. +31 of the stage
 struct StageScales {
-    uint16_t s[kKPerW][2];
-    uint8_t z[kKPerW][2];
+    uint16_t s[kKPerW];
+    uint8_t z[kKPerW];
 };
 
-__device__ __forceinline__ void load_stage_scales(const GemmParams &p, int n, int K0, StageScales &r)
+__device__ __forceinline__ void load_stage_scales(const GemmParams &p, int n, int K0, int h, StageScales &r)
 {
 #pragma unroll
-    for (int j = 0; j < kKPerW; ++j)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int g = (K0 + 64 * j + 32 * h) / p.group;
-            r.s[j][h] = 0;
-            r.z[j][h] = static_cast<uint8_t>(p.zero_const);
-            if (n < p.N && g < p.ng) {
-                r.s[j][h] = p.scales[static_cast<long long>(n) * p.ng + g];
-                if (p.zeros)
-                    r.z[j][h] = p.zeros[static_cast<long long>(n) * p.ng + g];
-            }
+    for (int j = 0; j < kKPerW; ++j) {
+        const int g = (K0 + 64 * j + 32 * h) / p.group;
+        r.s[j] = 0;
+        r.z[j] = static_cast<uint8_t>(p.zero_const);
+        if (n < p.N && g < p.ng) {
+            r.s[j] = p.scales[static_cast<long long>(n) * p.ng + g];
+            if (p.zeros)
+                r.z[j] = p.zeros[static_cast<long long>(n) * p.ng + g];
         }
+    }
 }
 
 __device__ __forceinline__ GroupConst group_const(uint16_t s_bits, uint8_t z, bool bf16)
@@ -393,22 +393,25 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUt
         }
         __syncwarp();
     } else if (warp >= kDeqWarp0) {
-        // ================= dequant: one thread per tile column =================
-        // Work goes by packed-weight stage (kKPerW K steps, unrolled so that the
-        // group of every 32 codes is known at compile time); the next stage's
-        // scales are loaded one stage ahead.
-        const int r = threadIdx.x - 32 * kDeqWarp0;     // 0..191
+        // ================= dequant: two threads per tile column =================
+        // Thread (r, h) turns codes 32h .. 32h + 31 of every 64 of column r into
+        // 16-bit values.  Work goes by packed-weight stage (kKPerW K steps,
+        // unrolled); the next stage's scales are loaded one stage ahead.
+        const int dt = threadIdx.x - 32 * kDeqWarp0;
+        const int r = dt % kBN;                         // column
+        const int qd = dt / kBN;                        // part of each 64 codes
+        const int h = qd * kDeqWords / 4;               // its half (the scale group of 32 codes)
         const int nws = (nks + kKPerW - 1) / kKPerW;
         int wi = 0, bi = 0;
         for (int tile = blockIdx.x; tile < p.tiles_n && ok; tile += gridDim.x) {
             const int n = tile * kBN + r;
             for (int pass = 0; pass < p.passes && ok; ++pass) {
                 StageScales nxt;
-                load_stage_scales(p, n, 0, nxt);
+                load_stage_scales(p, n, 0, h, nxt);
                 for (int wsi = 0; wsi < nws && ok; ++wsi) {
                     const StageScales cur = nxt;
                     if (wsi + 1 < nws)
-                        load_stage_scales(p, n, (wsi + 1) * kWK, nxt);
+                        load_stage_scales(p, n, (wsi + 1) * kWK, h, nxt);
                     const int ws = wi % kWStages;
                     if (!(ok = mbar_wait(&w_full[ws], (wi / kWStages) & 1, p.status)))
                         break;
@@ -420,18 +423,22 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUt
                             const int bs = bi % kBStages, bround = bi / kBStages;
                             if (bround > 0 && !(ok = mbar_wait(&b_empty[bs], (bround - 1) & 1, p.status)))
                                 break;
-                            // the 32 bytes (64 codes) of this column (rows of 128 B, swizzled)
-                            const uint4 p0 = *reinterpret_cast<const uint4 *>(wrow + (((2 * j) ^ (r & 7)) << 4));
-                            const uint4 p1 = *reinterpret_cast<const uint4 *>(wrow + (((2 * j + 1) ^ (r & 7)) << 4));
-                            const uint32_t wv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-                            const GroupConst ga = group_const(cur.s[j][0], cur.z[j][0], bf16);
-                            const GroupConst gb = group_const(cur.s[j][1], cur.z[j][1], bf16);
+                            // this part's words of the column's 64 codes (rows of 128 B, 16-byte
+                            // chunks swizzled); word i of the 64 codes sits in chunk 2j + i / 4
+                            uint32_t wv[kDeqWords];
+#pragma unroll
+                            for (int i = 0; i < kDeqWords; ++i) {
+                                const int wi = qd * kDeqWords + i;
+                                wv[i] = *reinterpret_cast<const uint32_t *>(
+                                    wrow + (((2 * j + (wi >> 2)) ^ (r & 7)) << 4) + 4 * (wi & 3));
+                            }
+                            const GroupConst gc = group_const(cur.s[j], cur.z[j], bf16);
                             uint8_t *brow = sb + bs * kBTileBytes + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
+                            for (int i = 0; i < kDeqWords; ++i) {
                                 uint32_t o[4];
-                                dequant_word4(wv[i], i < 4 ? ga : gb, bf16, o);
-                                *reinterpret_cast<uint4 *>(brow + ((i ^ (r & 7)) << 4)) =
+                                dequant_word4(wv[i], gc, bf16, o);
+                                *reinterpret_cast<uint4 *>(brow + (((qd * kDeqWords + i) ^ (r & 7)) << 4)) =
                                     make_uint4(o[0], o[1], o[2], o[3]);
                             }
                             fence_proxy_async_smem();
