@@ -268,6 +268,7 @@ def time_graph(torch, stream, launches, reps: int = 10):
             f()
     g.replay()
     stream.synchronize()
+    time.sleep(0.2)   # timed as a kernel alone: the burst peak applies
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         a.record(stream)
