@@ -34,7 +34,10 @@ static int plan_layout(GemvParams &p, int rb, int cp, int budget, int max_ring, 
     const int bar_bytes = align_up(kMaxRing * 12, 128);
     const int x_bytes = align_up(p.M * cp * 128 * 2, 128);
     const int xs_bytes = align_up(cp * ngc * MP * 4, 128);
-    const int sz_bytes = align_up(p.rbp * p.sz_pitch * 8, 128);   // float2 (s, z*s)
+    // scales as float2 (s, z*s) for one token tile, as stored (fp16 + uint8 zeros)
+    // for more, where activations and row blocks are large
+    p.sz_compact = token_tiles(p.M) >= 2;
+    const int sz_bytes = align_up(p.rbp * p.sz_pitch * (p.sz_compact ? (p.zeros ? 3 : 2) : 8), 128);
     const int red_bytes = align_up((1 << p.ksplit_log2) * p.rbp * MP * 4, 128);
     // group sums of x and of 2^E x
     const int fixed = 128 /* base alignment */ + bar_bytes + x_bytes + 2 * xs_bytes + sz_bytes + red_bytes + overrun;

@@ -36,6 +36,7 @@ struct GemvParams {
     int ksplit_log2;          // 8 warps = 2^ksplit_log2 K splits x (8 >> ksplit_log2) tile groups
     int ring, stage_bytes;    // pipeline slots and the bytes of one
     int off_bar, off_x, off_xs, off_cs, off_sz, off_red, off_ring, sz_pitch;
+    int sz_compact;           // scales staged as fp16 + uint8 zeros (M > 8), else float2 (s, z*s)
 };
 
 // Chooses grid, row blocking, K phases and the shared-memory layout.  A layout

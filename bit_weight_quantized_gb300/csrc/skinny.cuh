@@ -345,9 +345,10 @@ __device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t 
     }
 }
 
-// Scales and zero*scale of a block's rows as float2 (s, z*s): warp w takes rows
-// w, w + 8, ..., four rows' loads in flight per lane.
-static __device__ __noinline__ void stage_scales(const GemvParams &p, float2 *sz, int row0, int rows_valid)
+// Scales of a block's rows: as float2 (s, z*s), or as stored (fp16 scale, uint8
+// zero) when p.sz_compact.  Warp w takes rows w, w + 8, ..., four rows' loads in
+// flight per lane.
+static __device__ __noinline__ void stage_scales(const GemvParams &p, uint8_t *szb, int row0, int rows_valid)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ng = p.ng;
@@ -371,8 +372,15 @@ static __device__ __noinline__ void stage_scales(const GemvParams &p, float2 *sz
             for (int u = 0; u < 4; ++u) {
                 const int rr = r + u * kWarps;
                 if (rr < rows_valid) {
-                    const float sf = f16_bits_to_f32(sv[u]);
-                    sz[rr * p.sz_pitch + g] = make_float2(sf, static_cast<float>(zv[u]) * sf);
+                    const int o = rr * p.sz_pitch + g;
+                    if (p.sz_compact) {
+                        reinterpret_cast<uint16_t *>(szb)[o] = sv[u];
+                        if (p.zeros)
+                            szb[p.rbp * p.sz_pitch * 2 + o] = zv[u];
+                    } else {
+                        const float sf = f16_bits_to_f32(sv[u]);
+                        reinterpret_cast<float2 *>(szb)[o] = make_float2(sf, static_cast<float>(zv[u]) * sf);
+                    }
                 }
             }
         }
@@ -416,7 +424,7 @@ static __device__ __noinline__ void issue_stage(const GemvParams &p, int it, int
 }
 
 template <int B, int NT, int R, int MODE>
-__global__ void __launch_bounds__(kThreads, (NT == 1 || (NT == 2 && MODE == 0)) ? 2 : 1)
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
 skinny_kernel(const GemvParams p)
 {
     constexpr int MP = 8 * NT;                 // padded token count of the D fragments
@@ -432,7 +440,10 @@ skinny_kernel(const GemvParams p)
     uint16_t *xp = reinterpret_cast<uint16_t *>(smem + p.off_x);   // [chunk][group][M][4][R]
     float *xs = reinterpret_cast<float *>(smem + p.off_xs);        // [group][MP] sum x
     float *cs = reinterpret_cast<float *>(smem + p.off_cs);        // [group][MP] sum 2^E x
-    float2 *sz = reinterpret_cast<float2 *>(smem + p.off_sz);       // [row][sz_pitch] (s, z*s)
+    uint8_t *szb = smem + p.off_sz;   // scales: float2 (s, z*s) or fp16 + uint8 zeros, [row][sz_pitch]
+    const float2 *sz2 = reinterpret_cast<const float2 *>(szb);
+    const uint16_t *s16 = reinterpret_cast<const uint16_t *>(szb);
+    const uint8_t *z8 = szb + p.rbp * p.sz_pitch * 2;
     float *red = reinterpret_cast<float *>(smem + p.off_red);      // [ksplit][rbp][MP]
     uint8_t *ring = smem + p.off_ring;
 
@@ -465,7 +476,7 @@ skinny_kernel(const GemvParams p)
         for (int it = 0; it < first; ++it)
             issue_stage(p, it, it, ring, full, r0, nrows, policy);
     }
-    stage_scales(p, sz, r0, min(p.rb, nrows));
+    stage_scales(p, szb, r0, min(p.rb, nrows));
 
     // ---- the activations may come from the preceding kernel ----
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -497,7 +508,7 @@ skinny_kernel(const GemvParams p)
 
         if (blk > 0) {
             __syncthreads();   // the previous block's epilogue is done with sz / red
-            stage_scales(p, sz, row0, rows_valid);
+            stage_scales(p, szb, row0, rows_valid);
             __syncthreads();
         }
 
@@ -590,9 +601,15 @@ skinny_kernel(const GemvParams p)
 #pragma unroll
                                 for (int h = 0; h < 2; ++h) {
                                     load_run<B, R>(stage + roff[i][h], code0, w[i][h]);
-                                    const float2 v = sz[szo[i][h] + grp];
-                                    sc[i][h] = v.x;
-                                    zs[i][h] = v.y;
+                                    const int so = szo[i][h] + grp;
+                                    if constexpr (NT >= 2) {   // staged as stored (p.sz_compact)
+                                        sc[i][h] = f16_bits_to_f32(s16[so]);
+                                        zs[i][h] = (p.zeros ? static_cast<float>(z8[so]) : static_cast<float>(p.zero_const)) * sc[i][h];
+                                    } else {
+                                        const float2 v = sz2[so];
+                                        sc[i][h] = v.x;
+                                        zs[i][h] = v.y;
+                                    }
                                 }
                             uint32_t a0[NTL][R / 2], a1[NTL][R / 2];
 #pragma unroll
