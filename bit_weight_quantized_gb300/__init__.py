@@ -40,6 +40,7 @@ SIGNATURES = {
     "qmm_gemm": ([_P, _I, _P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P], _I),
     "qmm_w4a8": ([_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P], _I),
     "qmm_device_status": ([_P], _I),
+    "qmm_watchdog_selftest": ([_P], _I),
     "qmm_status_string": ([_I], ctypes.c_char_p),
     "qmm_abi_version": ([], _I),
 }
@@ -196,3 +197,10 @@ def qmm_status_string(status: int) -> str:
 
 def native_library_path() -> str:
     return LIB_PATH
+
+
+def qmm_watchdog_selftest(device=None):
+    """Runs the library's bounded-wait watchdog once on a wait that never
+    completes (about a second); qmm_device_status() then reports
+    QMM_ERR_TIMEOUT."""
+    _check(load().qmm_watchdog_selftest(_stream(device)), "qmm_watchdog_selftest")

@@ -16,6 +16,19 @@ namespace qmm {
 // The library's device status word (one per device that loads the library).
 __device__ int g_status_word = 0;
 
+// One warp waits on an mbarrier that nothing arrives at; the bounded wait gives
+// up, records QMM_ERR_TIMEOUT and the kernel returns.
+__global__ void watchdog_selftest_kernel(int *status)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    mbar_wait(&bar, 0, status);
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -319,6 +332,15 @@ qmm_status qmm_w4a8(const int8_t *xq, const void *sa, const uint8_t *w4, const v
     }
     return w4a8_dispatch(xq, sa, w4, ws, group, y, acc_out, M, N, K, f->status, f->num_sms,
                          f->smem_optin, f->smem_pair, stream);
+}
+
+qmm_status qmm_watchdog_selftest(cudaStream_t stream)
+{
+    const DeviceFacts *f = device_facts();
+    if (!f || f->usable != QMM_OK)
+        return QMM_ERR_DEVICE;
+    watchdog_selftest_kernel<<<1, 32, 0, stream>>>(f->status);
+    return from_cuda(cudaGetLastError());
 }
 
 qmm_status qmm_device_status(cudaStream_t stream)

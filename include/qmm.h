@@ -146,6 +146,15 @@ QMM_API qmm_status qmm_w4a8(const int8_t *xq, const void *sa, const uint8_t *w4,
  * pending asynchronous CUDA error is reported as QMM_ERR_CUDA. */
 QMM_API qmm_status qmm_device_status(cudaStream_t stream);
 
+/* Watchdog self-test (no counterpart in the pages; it exists to test failure
+ * detection without a GPU fault).  Launches one warp on `stream` that waits on
+ * a shared-memory mbarrier no thread ever arrives at, through the same bounded
+ * wait every qmm kernel uses: after about a second the wait gives up, records
+ * QMM_ERR_TIMEOUT in the device status word and the kernel returns normally.
+ * Returns QMM_OK if the launch succeeded; the following qmm_device_status()
+ * then reports QMM_ERR_TIMEOUT.  Touches no caller memory. */
+QMM_API qmm_status qmm_watchdog_selftest(cudaStream_t stream);
+
 /* Static, NUL-terminated description of a status code. */
 QMM_API const char *qmm_status_string(qmm_status status);
 
