@@ -83,7 +83,8 @@ _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(device=None):
-    # the raw handle of the current stream, without building a Stream object
+    # the raw handle of the current stream, without building a Stream object;
+    # `device` is a device index, a torch.device or None (the current device)
     if _raw_stream is not None:
         idx = device.index if isinstance(device, torch.device) else device
         if idx is None:
@@ -148,8 +149,9 @@ def _qmm(name, x, packed, bits, group, scales, zeros, zero_const, out, out_dtype
         out = torch.empty((M, N), dtype=out_dtype, device=x.device)
     _dev(out, "out", out_dtype, (M, N))
     fn = getattr(load(), name)
-    _check(fn(_ptr(x), _DT[x.dtype], _ptr(packed), bits, group, _ptr(scales), _ptr(zeros),
-              int(zero_const), _ptr(out), _DT[out_dtype], M, N, K, _stream(x.device)), name)
+    _check(fn(x.data_ptr(), _DT[x.dtype], packed.data_ptr(), bits, group, scales.data_ptr(),
+              None if zeros is None else zeros.data_ptr(), int(zero_const), out.data_ptr(),
+              _DT[out_dtype], M, N, K, _stream(x.get_device())), name)
     return out
 
 

@@ -3,6 +3,9 @@
 #include "gemv.h"
 #include "skinny.cuh"
 
+#include <mutex>
+#include <unordered_map>
+
 namespace qmm {
 
 static int align_up(int v, int a) { return (v + a - 1) / a * a; }
@@ -78,8 +81,8 @@ static void set_segment(GemvParams &p, int bits, int seg)
     p.stages_per_block = (p.nchunks + seg - 1) / seg;
 }
 
-qmm_status skinny_plan(GemvParams &p, int bits, int num_sms, int smem_max, int smem_pair,
-                       int *grid_out, int *smem_out)
+static qmm_status skinny_plan_search(GemvParams &p, int bits, int num_sms, int smem_max, int smem_pair,
+                                     int *grid_out, int *smem_out)
 {
     p.nchunks = (p.K + 127) / 128;
     int grid = (p.N + 15) / 16;
@@ -187,4 +190,96 @@ qmm_status skinny_plan(GemvParams &p, int bits, int num_sms, int smem_max, int s
     return QMM_ERR_UNSUPPORTED;
 }
 
+// The search above costs microseconds; decode calls repeat the same shapes, so
+// plans are kept per (shape, width, group, zero mode, device limits).
+namespace {
+
+struct PlanKey {
+    int M, N, K, bits, group, zeros, num_sms, smem_max, smem_pair;
+    bool operator==(const PlanKey &o) const
+    {
+        return M == o.M && N == o.N && K == o.K && bits == o.bits && group == o.group &&
+               zeros == o.zeros && num_sms == o.num_sms && smem_max == o.smem_max &&
+               smem_pair == o.smem_pair;
+    }
+};
+
+struct PlanKeyHash {
+    size_t operator()(const PlanKey &k) const
+    {
+        uint64_t h = 1469598103934665603ull;
+        const int v[9] = {k.M, k.N, k.K, k.bits, k.group, k.zeros, k.num_sms, k.smem_max, k.smem_pair};
+        for (int x : v) {
+            h ^= static_cast<uint32_t>(x);
+            h *= 1099511628211ull;
+        }
+        return static_cast<size_t>(h);
+    }
+};
+
+struct PlanEntry {
+    qmm_status status;
+    GemvParams plan;   // only the fields the search fills are used
+    int grid, smem;
+};
+
+std::mutex g_plan_mutex;
+std::unordered_map<PlanKey, PlanEntry, PlanKeyHash> g_plans;
+constexpr size_t kMaxPlans = 1024;
+
+void copy_plan_fields(GemvParams &d, const GemvParams &s)
+{
+    d.nchunks = s.nchunks;
+    d.stages_per_block = s.stages_per_block;
+    d.seg_chunks = s.seg_chunks;
+    d.seg_bytes = s.seg_bytes;
+    d.pitch = s.pitch;
+    d.phase_chunks = s.phase_chunks;
+    d.nphases = s.nphases;
+    d.rows_base = s.rows_base;
+    d.rows_rem = s.rows_rem;
+    d.rb = s.rb;
+    d.rbp = s.rbp;
+    d.ksplit_log2 = s.ksplit_log2;
+    d.ring = s.ring;
+    d.stage_bytes = s.stage_bytes;
+    d.off_bar = s.off_bar;
+    d.off_x = s.off_x;
+    d.off_xs = s.off_xs;
+    d.off_cs = s.off_cs;
+    d.off_sz = s.off_sz;
+    d.off_red = s.off_red;
+    d.off_ring = s.off_ring;
+    d.sz_pitch = s.sz_pitch;
+    d.sz_compact = s.sz_compact;
+}
+
+}  // namespace
+
+qmm_status skinny_plan(GemvParams &p, int bits, int num_sms, int smem_max, int smem_pair,
+                       int *grid_out, int *smem_out)
+{
+    const PlanKey key = {p.M, p.N, p.K, bits, p.group, p.zeros ? 1 : 0, num_sms, smem_max, smem_pair};
+    {
+        std::lock_guard<std::mutex> lock(g_plan_mutex);
+        auto it = g_plans.find(key);
+        if (it != g_plans.end()) {
+            copy_plan_fields(p, it->second.plan);
+            *grid_out = it->second.grid;
+            *smem_out = it->second.smem;
+            return it->second.status;
+        }
+    }
+    int grid = 0, smem = 0;
+    const qmm_status st = skinny_plan_search(p, bits, num_sms, smem_max, smem_pair, &grid, &smem);
+    std::lock_guard<std::mutex> lock(g_plan_mutex);
+    if (g_plans.size() >= kMaxPlans)
+        g_plans.clear();
+    g_plans[key] = PlanEntry{st, p, grid, smem};
+    *grid_out = grid;
+    *smem_out = smem;
+    return st;
+}
+
 }  // namespace qmm
+
