@@ -426,11 +426,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUt
                             // this part's words of the column's 64 codes (rows of 128 B, 16-byte
                             // chunks swizzled); word i of the 64 codes sits in chunk 2j + i / 4
                             uint32_t wv[kDeqWords];
+                            if constexpr (kDeqWords == 4) {   // one 16-byte chunk
+                                const uint4 v = *reinterpret_cast<const uint4 *>(
+                                    wrow + (((2 * j + qd) ^ (r & 7)) << 4));
+                                wv[0] = v.x; wv[1] = v.y; wv[2] = v.z; wv[3] = v.w;
+                            } else {
 #pragma unroll
-                            for (int i = 0; i < kDeqWords; ++i) {
-                                const int wi = qd * kDeqWords + i;
-                                wv[i] = *reinterpret_cast<const uint32_t *>(
-                                    wrow + (((2 * j + (wi >> 2)) ^ (r & 7)) << 4) + 4 * (wi & 3));
+                                for (int i = 0; i < kDeqWords; ++i) {
+                                    const int wi = qd * kDeqWords + i;
+                                    wv[i] = *reinterpret_cast<const uint32_t *>(
+                                        wrow + (((2 * j + (wi >> 2)) ^ (r & 7)) << 4) + 4 * (wi & 3));
+                                }
                             }
                             const GroupConst gc = group_const(cur.s[j], cur.z[j], bf16);
                             uint8_t *brow = sb + bs * kBTileBytes + (r >> 3) * 1024 + (r & 7) * 128;
