@@ -34,6 +34,7 @@ constexpr int kKPerW = kWK / kBK;  // K steps per packed-weight stage
 constexpr int kXStages = 3;
 constexpr int kWStages = 2;
 constexpr int kBStages = 3;
+static_assert(kXStages == kBStages, "x and B stages share their empty barriers");
 constexpr int kMTiles = 2;         // accumulators per pass
 constexpr int kAccCols = 256;      // TMEM column stride between the accumulators
 constexpr int kTmemCols = 512;
@@ -271,8 +272,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUt
     uint64_t *w_full = x_empty + kXStages;
     uint64_t *w_empty = w_full + kWStages;
     uint64_t *b_full = w_empty + kWStages;
-    uint64_t *b_empty = b_full + kBStages;
-    uint64_t *d_full = b_empty + kBStages;
+    // K step k uses x slot k % 3 and B slot k % 3: one barrier frees both (one
+    // MMA commit per K step)
+    uint64_t *b_empty = x_empty;
+    uint64_t *d_full = b_full + 2 * kBStages;
     uint64_t *d_empty = d_full + 1;
     uint64_t *drain = d_empty + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffTmemAddr);
@@ -292,7 +295,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUt
         }
         for (int i = 0; i < kBStages; ++i) {
             mbar_init(&b_full[i], kDeqWarps);
-            mbar_init(&b_empty[i], 1);
         }
         mbar_init(d_full, 1);
         mbar_init(d_empty, kEpiWarps);
@@ -355,7 +357,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUt
         // ================= MMA issuer =================
         if (lane == 0) {
             const uint32_t idesc = f16_idesc(bf16, kBM, kBN);
-            int xi = 0, bi = 0, np = 0;
+            // operand descriptors of slot 0, built once; the start-address field
+            // (bits 0..13, in 16-byte units; shared memory stays below 2^18 bytes) is
+            // advanced by the slot's offset and, per 16-wide K step, by 32 bytes (+2)
+            const uint64_t a_desc0 = sw128_desc(smem_u32(sx));
+            const uint64_t b_desc0 = sw128_desc(smem_u32(sb));
+            int slot = 0, np = 0;       // x and B stage slot (they advance together)
+            uint32_t parity = 0;
             for (int tile = blockIdx.x; tile < p.tiles_n && ok; tile += gridDim.x) {
                 for (int pass = 0; pass < p.passes && ok; ++pass) {
                     const int cnt = min(kMTiles, p.mtiles - pass * kMTiles);
@@ -363,24 +371,27 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUt
                         break;
                     tc_fence_after();
                     for (int ks = 0; ks < nks && ok; ++ks) {
-                        const int xs = xi % kXStages, bs = bi % kBStages;
-                        if (!(ok = mbar_wait(&x_full[xs], (xi / kXStages) & 1, p.status)))
+                        if (!(ok = mbar_wait(&x_full[slot], parity, p.status)))
                             break;
-                        if (!(ok = mbar_wait(&b_full[bs], (bi / kBStages) & 1, p.status)))
+                        if (!(ok = mbar_wait(&b_full[slot], parity, p.status)))
                             break;
                         tc_fence_after();
-                        const uint32_t b_base = smem_u32(sb + bs * kBTileBytes);
-                        for (int j = 0; j < cnt; ++j) {
-                            const uint32_t a_base = smem_u32(sx + (xs * kMTiles + j) * kXTileBytes);
+                        const uint32_t acc0 = ks > 0 ? 1u : 0u;
 #pragma unroll
-                            for (int kk = 0; kk < kBK / 16; ++kk)
-                                tc_mma(tmem_base + j * kAccCols, sw128_desc(a_base + kk * 32),
-                                       sw128_desc(b_base + kk * 32), idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+                        for (int j = 0; j < kMTiles; ++j) {
+                            if (j < cnt) {
+#pragma unroll
+                                for (int kk = 0; kk < kBK / 16; ++kk)
+                                    tc_mma(tmem_base + j * kAccCols,
+                                           a_desc0 + (((slot * kMTiles + j) * kXTileBytes) >> 4) + 2 * kk,
+                                           b_desc0 + ((slot * kBTileBytes) >> 4) + 2 * kk, idesc, kk > 0 ? 1u : acc0);
+                            }
                         }
-                        tc_commit(&x_empty[xs]);
-                        tc_commit(&b_empty[bs]);
-                        ++xi;
-                        ++bi;
+                        tc_commit(&x_empty[slot]);   // frees x slot and B slot
+                        if (++slot == kXStages) {
+                            slot = 0;
+                            parity ^= 1u;
+                        }
                     }
                     if (ok)
                         tc_commit(d_full);
