@@ -21,7 +21,7 @@ static int token_tiles(int M) { return M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 
 // Lays out shared memory for row blocks of `rb` rows, K phases of `cp` chunks and
 // at most `max_ring` slots; returns the dynamic shared-memory size, or 0 if
 // fewer than `min_ring` slots fit in `budget` bytes.
-static int plan_layout(GemvParams &p, int rb, int cp, int budget, int max_ring, int min_ring)
+static int plan_layout(GemvParams &p, int rb, int nblk, int cp, int budget, int max_ring, int min_ring)
 {
     const int MP = 8 * token_tiles(p.M);
     const int ngc = 128 / p.group;
@@ -43,7 +43,16 @@ static int plan_layout(GemvParams &p, int rb, int cp, int budget, int max_ring, 
     const int sz_bytes = align_up(p.rbp * p.sz_pitch * (p.sz_compact ? (p.zeros ? 3 : 2) : 8), 128);
     const int red_bytes = align_up((1 << p.ksplit_log2) * p.rbp * MP * 4, 128);
     // group sums of x and of 2^E x
-    const int fixed = 128 /* base alignment */ + bar_bytes + x_bytes + 2 * xs_bytes + sz_bytes + red_bytes + overrun;
+    int fixed = 128 /* base alignment */ + bar_bytes + x_bytes + 2 * xs_bytes + sz_bytes + red_bytes + overrun;
+    // The reduction buffer may reuse the activation buffer when the activations
+    // are not needed after a block's loop (one block, or restaged per phase); it
+    // costs a barrier, so it is taken only when it buys ring slots.
+    p.red_alias = 0;
+    if ((p.nphases > 1 || nblk == 1) && red_bytes <= x_bytes && (budget - fixed) / p.stage_bytes < max_ring &&
+        (budget - fixed + red_bytes) / p.stage_bytes > (budget - fixed) / p.stage_bytes) {
+        p.red_alias = 1;
+        fixed -= red_bytes;
+    }
     if (budget - fixed < p.stage_bytes * min_ring)
         return 0;
     int ring = (budget - fixed) / p.stage_bytes;
@@ -61,8 +70,9 @@ static int plan_layout(GemvParams &p, int rb, int cp, int budget, int max_ring, 
     off += xs_bytes;
     p.off_sz = off;
     off += sz_bytes;
-    p.off_red = off;
-    off += red_bytes;
+    p.off_red = p.red_alias ? p.off_x : off;
+    if (!p.red_alias)
+        off += red_bytes;
     p.off_ring = off;
     off += ring * p.stage_bytes + overrun;
     return off + 128;
@@ -96,18 +106,26 @@ static qmm_status skinny_plan_search(GemvParams &p, int bits, int num_sms, int s
     // a block holds at most 8 tiles of 16 rows (two per warp of a K split of 2)
     const int rbmax = 16 * kWarps * kTilesPerWarp / 2;
     const int nblk0 = (rows_max + rbmax - 1) / rbmax;
-    // K segment: about a kilobyte of each row per stage, at least 8 chunks
+    // K segment: about a kilobyte of each row per stage, at least 8 chunks; longer
+    // ones (up to 2 KB) are tried first, since fewer, larger bulk copies stream
+    // faster when the ring still holds as much
     int seg0 = (1024 + 16 * bits - 1) / (16 * bits);
     if (seg0 < 8)
         seg0 = 8;
     if (seg0 > p.nchunks)
         seg0 = p.nchunks;
+    int seg_hi = (2048 + 16 * bits - 1) / (16 * bits);
+    if (seg_hi < seg0)
+        seg_hi = seg0;
+    if (seg_hi > p.nchunks)
+        seg_hi = p.nchunks;
     const int budgets[2] = {smem_pair, smem_max};
     // Candidates are ranked by: how often the activations are staged (once with
     // one phase or one block, else once per block), row blocks (a block switch
     // drains the pipeline), phases, then bytes in flight (a shorter segment only
     // for at least 15% more), then segment length.  Segments under
-    // kMinSegBytes are tried only when nothing else fits.  A layout that lets
+    // kMinSegBytes, or not a multiple of the K split, are tried only when
+    // nothing else fits.  A layout that lets
     // two CTAs share an SM is taken first, if it needs one phase, the fewest
     // blocks and no short segments.
     struct Cand {
@@ -149,9 +167,13 @@ static qmm_status skinny_plan_search(GemvParams &p, int bits, int num_sms, int s
                     while (kl > 0 && tiles > kTilesPerWarp * (kWarps >> kl))
                         --kl;
                     p.ksplit_log2 = kl;
-                    for (int seg = seg0; seg >= 1; --seg) {
+                    for (int seg = seg_hi; seg >= 1; --seg) {
                         if (pass == 0 && seg < seg0 && seg * 16 * bits < kMinSegBytes)
                             break;
+                        // every warp of the K split gets the same number of a stage's
+                        // chunks (a stage ends when its slowest warp does)
+                        if (pass == 0 && seg < p.nchunks && seg % (1 << kl) != 0)
+                            continue;
                         set_segment(p, bits, seg);
                         // phase = a whole number of segments covering nchunks in nph phases
                         const int cp = ((p.stages_per_block + nph - 1) / nph) * seg;
@@ -159,7 +181,7 @@ static qmm_status skinny_plan_search(GemvParams &p, int bits, int num_sms, int s
                             continue;
                         const int total = nblk * p.stages_per_block;
                         const int max_ring = total < kMaxRing ? total : kMaxRing;
-                        if (!plan_layout(p, rb, cp, budget, max_ring, max_ring < 2 ? max_ring : 2))
+                        if (!plan_layout(p, rb, nblk, cp, budget, max_ring, max_ring < 2 ? max_ring : 2))
                             continue;
                         // bytes in flight from the start: the ring, or the whole slice if less
                         long long inflight = static_cast<long long>(p.ring) * p.seg_bytes;
@@ -181,7 +203,7 @@ static qmm_status skinny_plan_search(GemvParams &p, int bits, int num_sms, int s
                 const int cp = ((p.stages_per_block + best.nph - 1) / best.nph) * best.seg;
                 const int total = best.nblk * p.stages_per_block;
                 const int max_ring = total < kMaxRing ? total : kMaxRing;
-                *smem_out = plan_layout(p, rb, cp, budget, max_ring, max_ring < 2 ? max_ring : 2);
+                *smem_out = plan_layout(p, rb, best.nblk, cp, budget, max_ring, max_ring < 2 ? max_ring : 2);
                 *grid_out = grid;
                 return QMM_OK;
             }
@@ -252,6 +274,7 @@ void copy_plan_fields(GemvParams &d, const GemvParams &s)
     d.off_ring = s.off_ring;
     d.sz_pitch = s.sz_pitch;
     d.sz_compact = s.sz_compact;
+    d.red_alias = s.red_alias;
 }
 
 }  // namespace

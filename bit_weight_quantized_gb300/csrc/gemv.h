@@ -37,6 +37,7 @@ struct GemvParams {
     int ring, stage_bytes;    // pipeline slots and the bytes of one
     int off_bar, off_x, off_xs, off_cs, off_sz, off_red, off_ring, sz_pitch;
     int sz_compact;           // scales staged as fp16 + uint8 zeros (M > 8), else float2 (s, z*s)
+    int red_alias;            // the reduction buffer reuses the activation buffer
 };
 
 // Chooses grid, row blocking, K phases and the shared-memory layout.  A layout

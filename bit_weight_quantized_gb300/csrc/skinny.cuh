@@ -714,6 +714,8 @@ skinny_kernel(const GemvParams p)
         }
 
         // ---- cross-warp reduction in a fixed order, then the store ----
+        if (p.red_alias)
+            __syncthreads();   // every warp is done reading the activations it overwrites
 #pragma unroll
         for (int i = 0; i < TPW; ++i) {
             const int mt = tg + i * ntg;
