@@ -143,3 +143,23 @@ def test_skinny_full_size_sampled(q, M, N, bits):
     ref = oracle_y(prob, cols=cols)
     assert rel_err(y[:, cols], ref) <= REL_TOL
     _status_ok(q)
+
+
+# ---- row blocks: a CTA with more than 128 rows (N > 152 * 128) takes them in
+# blocks; with long K the activations are also staged in K phases, per block ----
+@pytest.mark.parametrize("M,N,K,bits,G,zm", [
+    (1, 20480, 512, 5, 64, "group"),
+    (3, 20000, 1024, 4, 128, "const8"),
+    (16, 19800, 8192, 3, 128, "half"),
+])
+def test_gemv_row_blocks_sampled(q, M, N, K, bits, G, zm):
+    prob = synthetic.make_qmm(M, N, K, bits, G, zero_mode=zm, seed=N + K)
+    y = y_to_f64(run_gemv(q, prob))
+    assert not np.isnan(y).any()
+    st = SplitMix64(N * 3 + K)
+    cols = (st.next(384) % np.uint64(N)).astype(np.int64)
+    # all rows of the first CTA (both of its blocks) and the last columns
+    cols = np.unique(np.concatenate([cols, np.arange(0, 140), [N - 2, N - 1]]))
+    ref = oracle_y(prob, cols=cols)
+    assert rel_err(y[:, cols], ref) <= REL_TOL
+    _status_ok(q)

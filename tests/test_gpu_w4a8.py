@@ -81,3 +81,16 @@ def test_w4a8_without_accumulators(q):
     y = q.qmm_w4a8(xq, sa, w4, ws, 128)
     y_ref, _, _ = oracle.solve_w4a8(prob, want_acc=False)
     assert rel_err(y.float().cpu().numpy().astype(np.float64), y_ref) <= REL_TOL
+
+
+def test_w4a8_row_blocks_sampled(q):
+    # more than 128 rows per CTA: two row blocks, accumulators still exact
+    prob = synthetic.make_w4a8(64, 20000, 1024, 128, seed=11)
+    y, acc = run(q, prob)
+    st = SplitMix64(20000)
+    cols = np.unique(np.concatenate([(st.next(256) % np.uint64(prob.N)).astype(np.int64),
+                                     np.arange(0, 140), [prob.N - 1]]))
+    y_ref, acc_ref, ov = oracle.solve_w4a8(prob, cols=cols)
+    assert not ov
+    np.testing.assert_array_equal(acc[:, cols, :], acc_ref)
+    assert rel_err(y[:, cols], y_ref) <= REL_TOL
