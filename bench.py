@@ -474,10 +474,31 @@ def run_ours(args, world, rank, local):
                 b_.record(stream)
             stream.synchronize()
             kdur[i] = a.elapsed_time(b_) / (8 * 16)
+    # isolated calls: each launch alone, after an L2 flush (a write of twice the
+    # L2), timed by events around it; median and min of 50 per width
+    flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.int32, device=dev)
+    iso = {}
+    with torch.cuda.stream(stream):
+        for i, p in enumerate(probs):
+            ts = []
+            for r in range(55):
+                flush.fill_(r)
+                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                pk, sc = sets[r % copies][i]
+                a.record(stream)
+                q.qmm_gemv(xs[i], pk, p.bits, p.group, sc, None, p.zero_const, out=ys[i])
+                b_.record(stream)
+                b_.synchronize()
+                if r >= 5:
+                    ts.append(a.elapsed_time(b_) * 1e3)
+            iso[str(p.bits)] = (statistics.median(ts), min(ts))
+    del flush
     per_width = {}
     for i, p in enumerate(probs):
         gb = p.algorithmic_bytes() / (kdur[i] * 1e-3) / 1e9
-        per_width[str(p.bits)] = {"us": round(kdur[i] * 1e3, 3), "GBps": round(gb, 1)}
+        med, mn = iso[str(p.bits)]
+        per_width[str(p.bits)] = {"us": round(kdur[i] * 1e3, 3), "GBps": round(gb, 1),
+                                  "isolated_us_median": round(med, 2), "isolated_us_min": round(mn, 2)}
     peak, peak_kind = measured_peaks()
     achieved = step_bytes / (kdur.sum() * 1e-3) / 1e9
     for k in per_width:
@@ -557,7 +578,10 @@ def run_ours(args, world, rank, local):
                          "traffic": traffic, "kernel": "qmm::skinny_kernel<b,1,32,0> (b = 1..8)",
                          "algorithmic_bytes_per_launch": round(step_bytes / len(probs)),
                          "frac_of_8TBs": round(achieved / 8000.0, 4),
-                         "duration_source": how},
+                         "duration_source": how,
+                         "per_width_note": "us / GBps: back-to-back launches (the roofline "
+                                           "durations); isolated_us_*: one launch after an L2 "
+                                           "flush, events around it, 50 runs"},
             "per_width": per_width,
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
