@@ -267,15 +267,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUt
     uint8_t *sw = smem + kOffW;
     uint8_t *sb = smem + kOffB;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
-    uint64_t *x_full = bars;
-    uint64_t *x_empty = x_full + kXStages;
+    // K step k uses x slot k % 3 and B slot k % 3.  One barrier per slot says both
+    // are full (the x tiles' bytes and the dequant warps' arrivals), one that both
+    // are free again (one MMA commit per K step).
+    uint64_t *b_full = bars;
+    uint64_t *x_empty = b_full + kBStages;
+    uint64_t *b_empty = x_empty;
     uint64_t *w_full = x_empty + kXStages;
     uint64_t *w_empty = w_full + kWStages;
-    uint64_t *b_full = w_empty + kWStages;
-    // K step k uses x slot k % 3 and B slot k % 3: one barrier frees both (one
-    // MMA commit per K step)
-    uint64_t *b_empty = x_empty;
-    uint64_t *d_full = b_full + 2 * kBStages;
+    uint64_t *d_full = w_empty + kWStages;
     uint64_t *d_empty = d_full + 1;
     uint64_t *drain = d_empty + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffTmemAddr);
@@ -285,16 +285,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUt
     const bool bf16 = p.bf16 != 0;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kXStages; ++i) {
-            mbar_init(&x_full[i], 1);
+        for (int i = 0; i < kXStages; ++i)
             mbar_init(&x_empty[i], 1);
-        }
         for (int i = 0; i < kWStages; ++i) {
             mbar_init(&w_full[i], 1);
             mbar_init(&w_empty[i], kDeqWarps);
         }
         for (int i = 0; i < kBStages; ++i) {
-            mbar_init(&b_full[i], kDeqWarps);
+            // the dequant warps' arrivals plus the producer's (with the x tiles' bytes)
+            mbar_init(&b_full[i], kDeqWarps + 1);
         }
         mbar_init(d_full, 1);
         mbar_init(d_empty, kEpiWarps);
@@ -336,9 +335,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUt
                         const int slot = xi % kXStages, round = xi / kXStages;
                         if (round > 0 && !(ok = mbar_wait(&x_empty[slot], (round - 1) & 1, p.status)))
                             break;
-                        mbar_arrive_expect_tx(&x_full[slot], cnt * kXTileBytes);
+                        mbar_arrive_expect_tx(&b_full[slot], cnt * kXTileBytes);
                         for (int j = 0; j < cnt; ++j)
-                            tma_load_2d(sx + (slot * kMTiles + j) * kXTileBytes, &tmx, &x_full[slot], ks * kBK,
+                            tma_load_2d(sx + (slot * kMTiles + j) * kXTileBytes, &tmx, &b_full[slot], ks * kBK,
                                         (mt0 + j) * kBM);
                         ++xi;
                     }
@@ -346,7 +345,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUt
             }
             // drain: the last copies into shared memory have landed
             for (int i = max(0, xi - kXStages); i < xi; ++i)
-                if (!mbar_wait(&x_full[i % kXStages], (i / kXStages) & 1, p.status))
+                if (!mbar_wait(&b_full[i % kXStages], (i / kXStages) & 1, p.status))
                     break;
             for (int i = max(0, wi - kWStages); i < wi; ++i)
                 if (!mbar_wait(&w_full[i % kWStages], (i / kWStages) & 1, p.status))
@@ -371,8 +370,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUt
                         break;
                     tc_fence_after();
                     for (int ks = 0; ks < nks && ok; ++ks) {
-                        if (!(ok = mbar_wait(&x_full[slot], parity, p.status)))
-                            break;
+                        // x tiles landed and the B tile written: one barrier
                         if (!(ok = mbar_wait(&b_full[slot], parity, p.status)))
                             break;
                         tc_fence_after();
