@@ -315,7 +315,7 @@ __device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t 
                         se[exp_of_code<B, R>(c)] += f16_bits_to_f32(v[u][c]);
 #pragma unroll
                     for (int e = 0; e < 11; ++e)
-                        csum += ldexpf(se[e], e);
+                        csum += se[e] * static_cast<float>(1 << e);   // exact: a power of two
                 }
                 // the run's R slots, contiguous: [chunk][group][token][quad thread][R]
                 uint16_t *dst = xp + ((static_cast<long long>(lc * NGC + gi) * M + m) * 4 + tt) * R;
@@ -732,12 +732,14 @@ skinny_kernel(const GemvParams p)
             }
         }
         __syncthreads();
+#pragma unroll 1
         for (int idx = threadIdx.x; idx < rows_valid * MP; idx += kThreads) {
             const int tok = idx & (MP - 1);
             const int row = idx / MP;   // MP is a power of two
             if (tok >= M)
                 continue;
             float v = 0.f;
+#pragma unroll 1
             for (int w = 0; w < ksplit; ++w)
                 v += red[(w * p.rbp + row) * MP + tok];
             if constexpr (MODE == 1)
