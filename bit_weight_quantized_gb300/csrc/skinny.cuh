@@ -406,16 +406,20 @@ static __device__ __noinline__ void issue_stage(const GemvParams &p, int it, int
         if (lane == 0)
             mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(rows_here * seg_len));
         __syncwarp();
+#pragma unroll 1
         for (int r = lane; r < rows_here; r += 32)
             bulk_load_hint(dst + r * p.pitch, src + static_cast<long long>(r) * p.row_bytes, seg_len,
                            &full[slot], policy);
     } else {
+        // rows one after another, the warp's lanes along the row
         const int words = seg_len / 4;
-        for (int e = lane; e < rows_here * words; e += 32) {
-            const int r = e / words;
-            const int wo = e - r * words;
-            *reinterpret_cast<uint32_t *>(dst + r * p.pitch + 4 * wo) =
-                *reinterpret_cast<const uint32_t *>(src + static_cast<long long>(r) * p.row_bytes + 4 * wo);
+#pragma unroll 1
+        for (int r = 0; r < rows_here; ++r) {
+            const uint32_t *srow = reinterpret_cast<const uint32_t *>(src + static_cast<long long>(r) * p.row_bytes);
+            uint32_t *drow = reinterpret_cast<uint32_t *>(dst + r * p.pitch);
+#pragma unroll 1
+            for (int wo = lane; wo < words; wo += 32)
+                drow[wo] = srow[wo];
         }
         __syncwarp();
         if (lane == 0)
