@@ -11,8 +11,8 @@
 // N = 28672 in one wave on 152 SMs) and walks the tokens in passes of two
 // 128-token M tiles, one TMEM accumulator each (2 x 192 of the 512 columns).
 // Per 64-wide K step: the x tiles (A operand, K-major, 128-byte swizzle) and,
-// every four K steps, a 192 x 256-code packed-weight tile arrive by TMA; six
-// dequant warps (one thread per weight column) turn 64 codes into bf16/fp16
+// every four K steps, a 192 x 256-code packed-weight tile arrive by TMA; twelve
+// dequant warps (two threads per weight column) turn 64 codes into bf16/fp16
 // (q - z) * s and write them in the same canonical K-major swizzled layout (B
 // operand); one thread issues 4 x 2 MMAs of K = 16; four epilogue warps move
 // the accumulators TMEM -> registers -> global memory.  The roles meet on
@@ -66,6 +66,8 @@ struct GemmParams {
     uint16_t *y;              // [M][N]
     int *status;
     int M, N, K, group, ng, zero_const, bf16;
+    int group_log2;           // G = 1 << group_log2
+    int vec_scales;           // scale rows 16-byte aligned and ng % 8 == 0 (zeros 8-byte aligned)
     int tiles_n, mtiles, passes, ksteps;
 };
 
@@ -197,26 +199,57 @@ struct GroupConst {
     uint32_t off2;
 };
 
-// raw scale / zero of the groups of one half (32 codes of every 64) of a
-// packed-weight stage: entry [j] covers codes 64j + 32h .. +31 of the stage
-struct StageScales {
-    uint16_t s[kKPerW];
-    uint8_t z[kKPerW];
+// Scales and zeros of eight consecutive groups 8w .. 8w + 7 of one column, held
+// in registers.  Where the rows allow it one 16-byte load (and one 8-byte load
+// of the zeros) fetches the window: a warp's 32 columns are 32 different rows,
+// so scattered 2-byte loads would cost the L1 data pipe one wavefront per
+// column per group, the same pipe the B-tile stores use.
+struct ScaleWindow {
+    uint4 s;   // fp16 scale of group 8w + i in half (i & 1) of word i / 2
+    uint2 z;   // zero of group 8w + i in byte (i & 3) of word i / 4
 };
 
-__device__ __forceinline__ void load_stage_scales(const GemmParams &p, int n, int K0, int h, StageScales &r)
+__device__ __forceinline__ void load_window(const GemmParams &p, int n, int w, ScaleWindow &r)
 {
+    const int g0 = 8 * w;
+    const uint32_t zc = static_cast<uint32_t>(p.zero_const) * 0x01010101u;
+    r.s = make_uint4(0u, 0u, 0u, 0u);
+    r.z = make_uint2(zc, zc);
+    if (n >= p.N || g0 >= p.ng)
+        return;
+    const long long base = static_cast<long long>(n) * p.ng + g0;
+    if (p.vec_scales) {   // 16-byte aligned rows, ng % 8 == 0: the window lies inside the row
+        r.s = *reinterpret_cast<const uint4 *>(p.scales + base);
+        if (p.zeros)
+            r.z = *reinterpret_cast<const uint2 *>(p.zeros + base);
+        return;
+    }
+    uint32_t sw[4] = {0u, 0u, 0u, 0u};
+    uint32_t zw[2] = {zc, zc};
 #pragma unroll
-    for (int j = 0; j < kKPerW; ++j) {
-        const int g = (K0 + 64 * j + 32 * h) / p.group;
-        r.s[j] = 0;
-        r.z[j] = static_cast<uint8_t>(p.zero_const);
-        if (n < p.N && g < p.ng) {
-            r.s[j] = p.scales[static_cast<long long>(n) * p.ng + g];
-            if (p.zeros)
-                r.z[j] = p.zeros[static_cast<long long>(n) * p.ng + g];
+    for (int i = 0; i < 8; ++i) {
+        if (g0 + i >= p.ng)
+            break;
+        sw[i >> 1] |= static_cast<uint32_t>(p.scales[base + i]) << (16 * (i & 1));
+        if (p.zeros) {
+            const int sh = 8 * (i & 3);
+            zw[i >> 2] = (zw[i >> 2] & ~(0xFFu << sh)) | (static_cast<uint32_t>(p.zeros[base + i]) << sh);
         }
     }
+    r.s = make_uint4(sw[0], sw[1], sw[2], sw[3]);
+    r.z = make_uint2(zw[0], zw[1]);
+}
+
+__device__ __forceinline__ uint16_t window_scale(const ScaleWindow &w, int i)
+{
+    const uint32_t a = (i & 4) ? ((i & 2) ? w.s.w : w.s.z) : ((i & 2) ? w.s.y : w.s.x);
+    return static_cast<uint16_t>((i & 1) ? (a >> 16) : (a & 0xFFFFu));
+}
+
+__device__ __forceinline__ uint8_t window_zero(const ScaleWindow &w, int i)
+{
+    const uint32_t a = (i & 4) ? w.z.y : w.z.x;
+    return static_cast<uint8_t>(a >> (8 * (i & 3)));
 }
 
 __device__ __forceinline__ GroupConst group_const(uint16_t s_bits, uint8_t z, bool bf16)
@@ -405,7 +438,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUt
         // ================= dequant: two threads per tile column =================
         // Thread (r, h) turns codes 32h .. 32h + 31 of every 64 of column r into
         // 16-bit values.  Work goes by packed-weight stage (kKPerW K steps,
-        // unrolled); the next stage's scales are loaded one stage ahead.
+        // unrolled).  Scales come from a register window of eight groups, the
+        // next window loaded one window ahead.
         const int dt = threadIdx.x - 32 * kDeqWarp0;
         const int r = dt % kBN;                         // column
         const int qd = dt / kBN;                        // part of each 64 codes
@@ -415,12 +449,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUt
         for (int tile = blockIdx.x; tile < p.tiles_n && ok; tile += gridDim.x) {
             const int n = tile * kBN + r;
             for (int pass = 0; pass < p.passes && ok; ++pass) {
-                StageScales nxt;
-                load_stage_scales(p, n, 0, h, nxt);
+                // group g = (64 ks + 32 h) / G grows by at most 2 per K step (G >= 32),
+                // so the window index g / 8 grows by at most one
+                ScaleWindow cur, nxt;
+                int wcur = 0;
+                load_window(p, n, 0, cur);
+                load_window(p, n, 1, nxt);
                 for (int wsi = 0; wsi < nws && ok; ++wsi) {
-                    const StageScales cur = nxt;
-                    if (wsi + 1 < nws)
-                        load_stage_scales(p, n, (wsi + 1) * kWK, h, nxt);
                     const int ws = wi % kWStages;
                     if (!(ok = mbar_wait(&w_full[ws], (wi / kWStages) & 1, p.status)))
                         break;
@@ -447,7 +482,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUt
                                         wrow + (((2 * j + (wi >> 2)) ^ (r & 7)) << 4) + 4 * (wi & 3));
                                 }
                             }
-                            const GroupConst gc = group_const(cur.s[j], cur.z[j], bf16);
+                            const int g = (64 * ks + 32 * h) >> p.group_log2;
+                            if ((g >> 3) != wcur) {
+                                cur = nxt;
+                                ++wcur;
+                                load_window(p, n, wcur + 1, nxt);
+                            }
+                            const GroupConst gc = group_const(window_scale(cur, g & 7), window_zero(cur, g & 7), bf16);
                             uint8_t *brow = sb + bs * kBTileBytes + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
                             for (int i = 0; i < kDeqWords; ++i) {
@@ -534,6 +575,8 @@ qmm_status gemm_dispatch(const void *x, bool x_bf16, const uint8_t *packed, int 
 {
     if (bits != 4)
         return QMM_ERR_UNSUPPORTED;   // the tiled path dequantizes 4-bit codes
+    if (group != 32 && group != 64 && group != 128)
+        return QMM_ERR_SHAPE;
     const long long row_bytes = static_cast<long long>(K) * bits / 8;
     if (reinterpret_cast<uintptr_t>(packed) % 16 || row_bytes % 16 ||
         reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(y) % 16)
@@ -560,6 +603,9 @@ qmm_status gemm_dispatch(const void *x, bool x_bf16, const uint8_t *packed, int 
     p.ng = K / group;
     p.zero_const = zeros ? 0 : zero_const;
     p.bf16 = x_bf16 ? 1 : 0;
+    p.group_log2 = group == 32 ? 5 : group == 64 ? 6 : 7;
+    p.vec_scales = reinterpret_cast<uintptr_t>(scales) % 16 == 0 && p.ng % 8 == 0 &&
+                   (!zeros || reinterpret_cast<uintptr_t>(zeros) % 8 == 0);
     p.tiles_n = (N + kBN - 1) / kBN;
     p.mtiles = (M + kBM - 1) / kBM;
     p.passes = (p.mtiles + kMTiles - 1) / kMTiles;

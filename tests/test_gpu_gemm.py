@@ -90,3 +90,30 @@ def test_tiled_full_size_sampled(q, M):
     rows = np.concatenate([rows, [0, M - 1]])
     ref = oracle_y(prob, rows=rows, cols=cols)
     check(prob, y[np.ix_(rows, cols)], ref)
+
+
+def _misaligned_copy(t, shift):
+    """A contiguous copy of `t` whose data starts `shift` elements past an
+    allocation boundary (so not 16-byte aligned)."""
+    flat = torch.empty(t.numel() + 16, dtype=t.dtype, device=t.device)
+    view = flat[shift:shift + t.numel()]
+    view.copy_(t.reshape(-1))
+    return view.view(t.shape)
+
+
+@pytest.mark.parametrize("M,N,K,G,dt", [(40, 200, 640, 64, "bf16"), (24, 130, 1024, 32, "f16"),
+                                        (64, 250, 2048, 128, "bf16")])
+def test_gemm_unaligned_scale_rows(q, M, N, K, G, dt):
+    """Scales and zeros whose rows are not 16-byte aligned (and K / G not a
+    multiple of 8 in the first case) take the scalar scale loads."""
+    prob = synthetic.make_qmm(M, N, K, 4, G, zero_mode="group", x_dtype=dt, y_dtype=dt,
+                              seed=M + N + K)
+    x, packed, scales, zeros = to_dev_problem(prob)
+    scales = _misaligned_copy(scales, 1)
+    zeros = _misaligned_copy(zeros, 3)
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float16
+    y = torch.full((M, N), float("nan"), dtype=tdt, device="cuda")
+    q.qmm_gemm(x, packed, 4, G, scales, zeros, 0, out=y)
+    torch.cuda.synchronize()
+    assert q.qmm_device_status() == 0
+    check(prob, y_to_f64(y), oracle_y(prob))
