@@ -31,11 +31,7 @@ constexpr int kBM = 128;           // tokens per M tile (MMA M)
 constexpr int kBK = 64;            // K per step: one 128-byte swizzle atom of 16-bit values
 constexpr int kWK = 256;           // codes per packed-weight stage (128 bytes per row at b = 4)
 constexpr int kKPerW = kWK / kBK;  // K steps per packed-weight stage
-constexpr int kXStages = 3;
 constexpr int kWStages = 2;
-constexpr int kBStages = 3;
-static_assert(kXStages == kBStages, "x and B stages share their empty barriers");
-constexpr int kMTiles = 2;         // accumulators per pass
 constexpr int kAccCols = 256;      // TMEM column stride between the accumulators
 constexpr int kTmemCols = 512;
 
@@ -52,13 +48,24 @@ constexpr int kXTileBytes = kBM * kBK * 2;     // 16 KB
 constexpr int kWTileBytes = kBN * 128;          // 24 KB
 constexpr int kBTileBytes = kBN * kBK * 2;      // 24 KB
 
-constexpr int kOffX = 0;
-constexpr int kOffW = kOffX + kXStages * kMTiles * kXTileBytes;
-constexpr int kOffB = kOffW + kWStages * kWTileBytes;
-constexpr int kOffBar = kOffB + kBStages * kBTileBytes;
-constexpr int kNumBars = 2 * kXStages + 2 * kWStages + 2 * kBStages + 3;
-constexpr int kOffTmemAddr = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffTmemAddr + 16 + 1024;   // + alignment slack
+// Shared-memory layout of one configuration: MT accumulators (128-token M
+// tiles) per pass and S stages of x tiles and of B tiles (x and B stages share
+// their empty barriers, so they advance together).  Two configurations exist:
+// <2, 3> for M > 128, and <1, 4> for M <= 128, which spends the room of the
+// unused second x tile on a fourth stage.
+template <int MT, int S>
+struct Layout {
+    static constexpr int kOffX = 0;
+    static constexpr int kOffW = kOffX + S * MT * kXTileBytes;
+    static constexpr int kOffB = kOffW + kWStages * kWTileBytes;
+    static constexpr int kOffBar = kOffB + S * kBTileBytes;
+    // b_full [S], x_empty (= b_empty) [S], w_full / w_empty [kWStages], d_full, d_empty, drain
+    static constexpr int kNumBars = 2 * S + 2 * kWStages + 3;
+    static constexpr int kOffTmemAddr = kOffBar + kNumBars * 8;
+    static constexpr int kBytes = kOffTmemAddr + 16 + 1024;   // + alignment slack
+};
+static_assert(Layout<2, 3>::kBytes <= 227 * 1024 && Layout<1, 4>::kBytes <= 227 * 1024,
+              "shared memory per CTA");
 
 struct GemmParams {
     const uint16_t *scales;   // fp16 [N][K/G]
@@ -289,17 +296,22 @@ __device__ __forceinline__ void dequant_word4(uint32_t w, const GroupConst &c, b
     }
 }
 
+template <int MT, int S>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
             const GemmParams p)
 {
+    constexpr int kMTiles = MT;   // accumulators per pass
+    constexpr int kXStages = S;
+    constexpr int kBStages = S;
+    using L = Layout<MT, S>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    uint8_t *sx = smem + kOffX;
-    uint8_t *sw = smem + kOffW;
-    uint8_t *sb = smem + kOffB;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint8_t *sx = smem + L::kOffX;
+    uint8_t *sw = smem + L::kOffW;
+    uint8_t *sb = smem + L::kOffB;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
     // K step k uses x slot k % 3 and B slot k % 3.  One barrier per slot says both
     // are full (the x tiles' bytes and the dequant warps' arrivals), one that both
     // are free again (one MMA commit per K step).
@@ -311,7 +323,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUt
     uint64_t *d_full = w_empty + kWStages;
     uint64_t *d_empty = d_full + 1;
     uint64_t *drain = d_empty + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffTmemAddr);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffTmemAddr);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -566,6 +578,38 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUt
         tmem_dealloc(tmem_base, kTmemCols);
 }
 
+template <int MT, int S>
+qmm_status launch_gemm(const CUtensorMap &tmx, const CUtensorMap &tmw, GemmParams p, int grid,
+                       int smem_optin, cudaStream_t stream)
+{
+    constexpr int smem = Layout<MT, S>::kBytes;
+    if (smem_optin < smem)
+        return QMM_ERR_UNSUPPORTED;
+    p.passes = (p.mtiles + MT - 1) / MT;
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        if (cudaFuncSetAttribute(gemm_kernel<MT, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+            return QMM_ERR_CUDA;
+        configured[dev] = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, gemm_kernel<MT, S>, tmx, tmw, p) != cudaSuccess)
+        return QMM_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+}
+
 }  // namespace
 
 qmm_status gemm_dispatch(const void *x, bool x_bf16, const uint8_t *packed, int bits, int group,
@@ -581,8 +625,6 @@ qmm_status gemm_dispatch(const void *x, bool x_bf16, const uint8_t *packed, int 
     if (reinterpret_cast<uintptr_t>(packed) % 16 || row_bytes % 16 ||
         reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(y) % 16)
         return QMM_ERR_ALIGN;
-    if (smem_optin < kSmemBytes)
-        return QMM_ERR_UNSUPPORTED;
     CUtensorMap tmx, tmw;
     std::memset(&tmx, 0, sizeof(tmx));
     std::memset(&tmw, 0, sizeof(tmw));
@@ -608,32 +650,11 @@ qmm_status gemm_dispatch(const void *x, bool x_bf16, const uint8_t *packed, int 
                    (!zeros || reinterpret_cast<uintptr_t>(zeros) % 8 == 0);
     p.tiles_n = (N + kBN - 1) / kBN;
     p.mtiles = (M + kBM - 1) / kBM;
-    p.passes = (p.mtiles + kMTiles - 1) / kMTiles;
     p.ksteps = (K + kBK - 1) / kBK;
-    int grid = p.tiles_n < num_sms ? p.tiles_n : num_sms;
-
-    static int configured[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-        if (cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-            cudaSuccess)
-            return QMM_ERR_CUDA;
-        configured[dev] = 1;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, gemm_kernel, tmx, tmw, p) != cudaSuccess)
-        return QMM_ERR_CUDA;
-    return cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+    const int grid = p.tiles_n < num_sms ? p.tiles_n : num_sms;
+    if (p.mtiles == 1)
+        return launch_gemm<1, 4>(tmx, tmw, p, grid, smem_optin, stream);
+    return launch_gemm<2, 3>(tmx, tmw, p, grid, smem_optin, stream);
 }
 
 }  // namespace qmm
