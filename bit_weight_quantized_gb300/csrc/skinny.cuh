@@ -203,19 +203,22 @@ __device__ __forceinline__ constexpr int code_of_slot(int s)
     }
 }
 
-__device__ __forceinline__ uint16_t s8_to_f16_bits(int v)
+// Four int8 values (one word) -> two fp16x2 words, exactly: with u = x + 128
+// (the sign bit flipped), the byte permute forms fp16 1024 + u under the
+// exponent byte 0x64, and subtracting 1152 leaves x.
+__device__ __forceinline__ void s8x4_to_f16x2(uint32_t w, uint32_t &lo, uint32_t &hi)
 {
-    uint16_t h;
-    asm("cvt.rn.f16.s32 %0, %1;" : "=h"(h) : "r"(v));
-    return h;
+    const uint32_t u = w ^ 0x80808080u;
+    lo = hsub2(prmt(u, 0x64646464u, 0x4140u), 0x64806480u);
+    hi = hsub2(prmt(u, 0x64646464u, 0x4342u), 0x64806480u);
 }
 
 // Loads run `idx` (R codes of one token) of the chunks [ch0, ch0 + nch) as fp16
-// bit patterns; returns false past the end.  MODE 0 reads fp16 x, MODE 1 int8 xq
-// (converted exactly).
+// bit patterns (zeros past K).  MODE 0 reads fp16 x; MODE 1 reads int8 xq,
+// converts it exactly and also returns the run's integer sum in `isum`.
 template <int R, int MODE>
 __device__ __forceinline__ void load_act_run(const GemvParams &p, int ch0, int runs_per_tok,
-                                             int idx, uint16_t (&v)[R])
+                                             int idx, uint16_t (&v)[R], int &isum)
 {
     constexpr int G = 4 * R;
     constexpr int RPC = 128 / R;                 // runs per chunk
@@ -234,15 +237,21 @@ __device__ __forceinline__ void load_act_run(const GemvParams &p, int ch0, int r
             v[c + 6] = q.w & 0xFFFF; v[c + 7] = q.w >> 16;
         }
     } else {
+        isum = 0;
 #pragma unroll
         for (int c = 0; c < R; c += 8) {
             uint2 q = make_uint2(0, 0);
             if (k0 + c < p.K)
                 q = *reinterpret_cast<const uint2 *>(p.xq + static_cast<long long>(m) * p.K + k0 + c);
+            isum = __dp4a(static_cast<int>(q.x), 0x01010101, isum);
+            isum = __dp4a(static_cast<int>(q.y), 0x01010101, isum);
+            uint32_t h[4];
+            s8x4_to_f16x2(q.x, h[0], h[1]);
+            s8x4_to_f16x2(q.y, h[2], h[3]);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const uint32_t word = e < 4 ? q.x : q.y;
-                v[c + e] = s8_to_f16_bits(static_cast<int>(static_cast<int8_t>((word >> (8 * (e & 3))) & 0xFF)));
+            for (int e = 0; e < 4; ++e) {
+                v[c + 2 * e] = static_cast<uint16_t>(h[e] & 0xFFFFu);
+                v[c + 2 * e + 1] = static_cast<uint16_t>(h[e] >> 16);
             }
         }
     }
@@ -276,10 +285,13 @@ __device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t 
     // warp-uniform trip count: the quad shuffles need every lane
     for (int wbase = threadIdx.x - lane; wbase < nruns; wbase += U * kThreads) {
         uint16_t v[U][R];
+        int isum[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u)
+        for (int u = 0; u < U; ++u) {
+            isum[u] = 0;
             if (wbase + lane + u * kThreads < nruns)
-                load_act_run<R, MODE>(p, ch0, runs_per_tok, wbase + lane + u * kThreads, v[u]);
+                load_act_run<R, MODE>(p, ch0, runs_per_tok, wbase + lane + u * kThreads, v[u], isum[u]);
+        }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int idx = wbase + lane + u * kThreads;
@@ -292,18 +304,20 @@ __device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t 
                 lc = rr / RPC;
                 gi = (rr % RPC) / 4;
                 tt = rr % 4;
-                // pairwise, in a fixed order (exact for int8 inputs)
-                float ps[R];
+                if constexpr (MODE == 1) {
+                    sum = static_cast<float>(isum[u]);   // exact: |sum| <= 128 R
+                } else {
+                    // pairwise, in a fixed order
+                    float ps[R];
 #pragma unroll
-                for (int c = 0; c < R; ++c)
-                    ps[c] = f16_bits_to_f32(v[u][c]);
+                    for (int c = 0; c < R; ++c)
+                        ps[c] = f16_bits_to_f32(v[u][c]);
 #pragma unroll
-                for (int w = 1; w < R; w *= 2)
+                    for (int w = 1; w < R; w *= 2)
 #pragma unroll
-                    for (int c = 0; c < R; c += 2 * w)
-                        ps[c] += ps[c + w];
-                sum = ps[0];
-                if constexpr (MODE == 0) {
+                        for (int c = 0; c < R; c += 2 * w)
+                            ps[c] += ps[c + w];
+                    sum = ps[0];
                     // sum_k 2^E_k x_k: x summed per exponent, then scaled (exact)
                     // and added in increasing exponent order
                     float se[11];
