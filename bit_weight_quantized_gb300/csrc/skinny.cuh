@@ -257,6 +257,18 @@ __device__ __forceinline__ void load_act_run(const GemvParams &p, int ch0, int r
     }
 }
 
+// Chunk swizzle of the staged activations.  A run of R fp16 slots is R / 8
+// 16-byte chunks; the run of (token, quad thread) index i stores its chunk c at
+// chunk c ^ act_swizzle<R>(i).  Without it the 32 lanes of a fragment load (runs
+// i = 0..31, the same chunk) would hit only 128 / (2 R) distinct 16-byte bank
+// groups; with it every wavefront of 16-byte loads is conflict-free.
+template <int R>
+__device__ __forceinline__ int act_swizzle(int i)
+{
+    constexpr int NCH = R / 8;                   // chunks per run
+    return NCH > 1 ? (i / (8 / NCH)) & (NCH - 1) : 0;
+}
+
 // Stages the activations of chunks [ch0, ch0 + nch) in slot order, and the
 // per-group sums X[group][token]: each run summed pairwise in a fixed order,
 // the four runs of a group added in order across the quad's lanes, so the
@@ -331,8 +343,9 @@ __device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t 
                     for (int e = 0; e < 11; ++e)
                         csum += se[e] * static_cast<float>(1 << e);   // exact: a power of two
                 }
-                // the run's R slots, contiguous: [chunk][group][token][quad thread][R]
+                // the run's R slots: [chunk][group][token][quad thread][R], chunks swizzled
                 uint16_t *dst = xp + ((static_cast<long long>(lc * NGC + gi) * M + m) * 4 + tt) * R;
+                const int swz = act_swizzle<R>(m * 4 + tt);
 #pragma unroll
                 for (int j = 0; j < R / 4; j += 2) {
                     uint4 o;
@@ -340,7 +353,7 @@ __device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t 
                     o.y = v[u][code_of_slot<B, R>(4 * j + 2)] | (static_cast<uint32_t>(v[u][code_of_slot<B, R>(4 * j + 3)]) << 16);
                     o.z = v[u][code_of_slot<B, R>(4 * j + 4)] | (static_cast<uint32_t>(v[u][code_of_slot<B, R>(4 * j + 5)]) << 16);
                     o.w = v[u][code_of_slot<B, R>(4 * j + 6)] | (static_cast<uint32_t>(v[u][code_of_slot<B, R>(4 * j + 7)]) << 16);
-                    *reinterpret_cast<uint4 *>(dst + 4 * j) = o;
+                    *reinterpret_cast<uint4 *>(dst + 8 * ((j >> 1) ^ swz)) = o;
                 }
             }
             const float s1 = __shfl_down_sync(0xffffffffu, sum, 1);
@@ -506,14 +519,18 @@ skinny_kernel(const GemvParams p)
     const int g = lane >> 2, t = lane & 3;
     const int M = p.M;
     const int ng = p.ng;
-    // activation fragments of token g + 8 nt and quad thread t: R contiguous slots at
-    // xp[(chunk * NGC + group) * M * 4 R + xlane[nt]]; tokens past M read token M - 1
-    // (their accumulator columns are never stored)
+    // activation fragments of token g + 8 nt and quad thread t: R slots at
+    // xp[(chunk * NGC + group) * M * 4 R + xlane[nt]], 16-byte chunks swizzled by
+    // xswz[nt]; tokens past M read token M - 1 (their accumulator columns are never
+    // stored)
     const int gstride = M * 4 * R;
-    int xlane[NT];
+    int xlane[NT], xswz[NT];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-        xlane[nt] = (min(g + 8 * nt, M - 1) * 4 + t) * R;
+    for (int nt = 0; nt < NT; ++nt) {
+        const int i = min(g + 8 * nt, M - 1) * 4 + t;
+        xlane[nt] = i * R;
+        xswz[nt] = act_swizzle<R>(i);
+    }
 
     bool ok = true;
     int it = 0;                 // pipeline stage, and its slot and phase parity
@@ -596,7 +613,7 @@ skinny_kernel(const GemvParams p)
                                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                                     for (int j = 0; j < R / 4; j += 2) {
-                                        const uint4 v = *reinterpret_cast<const uint4 *>(xg + xlane[nt] + 4 * j);
+                                        const uint4 v = *reinterpret_cast<const uint4 *>(xg + xlane[nt] + 8 * ((j >> 1) ^ xswz[nt]));
                                         bf[j][nt][0] = v.x;
                                         bf[j][nt][1] = v.y;
                                         bf[j + 1][nt][0] = v.z;
@@ -646,15 +663,17 @@ skinny_kernel(const GemvParams p)
                                     for (int e = 0; e < 4; ++e)
                                         d[i][0][e] = d[i][1][e] = 0.f;
 #pragma unroll
+                                uint4 bv = make_uint4(0u, 0u, 0u, 0u);   // NT > 2: chunk of j, j + 1
                                 for (int j = 0; j < R / 4; ++j) {
                                     uint32_t b0, b1;
                                     if constexpr (NT <= 2) {
                                         b0 = bf[j][nt][0];
                                         b1 = bf[j][nt][1];
                                     } else {
-                                        const uint2 v = *reinterpret_cast<const uint2 *>(xg + xlane[nt] + 4 * j);
-                                        b0 = v.x;
-                                        b1 = v.y;
+                                        if ((j & 1) == 0)
+                                            bv = *reinterpret_cast<const uint4 *>(xg + xlane[nt] + 8 * ((j >> 1) ^ xswz[nt]));
+                                        b0 = (j & 1) ? bv.z : bv.x;
+                                        b1 = (j & 1) ? bv.w : bv.y;
                                     }
 #pragma unroll
                                     for (int i = 0; i < NTL; ++i)
