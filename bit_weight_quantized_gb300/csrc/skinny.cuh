@@ -294,20 +294,26 @@ __device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t 
                 cs[lg * MP + M + (idx - lg * (MP - M))] = 0.f;
         }
     }
+    // With at most half as many runs as threads, the runs go to every other lane
+    // of all eight warps (two warps per scheduler instead of one).
+    const int sp = 2 * nruns <= kThreads ? 2 : 1;
+    const int rpw = 32 / sp;                         // runs per warp and pass
+    const int rstep = kWarps * rpw;
+    const int mylane = (lane % sp == 0) ? lane / sp : rpw;   // rpw: no run
     // warp-uniform trip count: the quad shuffles need every lane
-    for (int wbase = threadIdx.x - lane; wbase < nruns; wbase += U * kThreads) {
+    for (int wbase = (threadIdx.x >> 5) * rpw; wbase < nruns; wbase += U * rstep) {
         uint16_t v[U][R];
         int isum[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             isum[u] = 0;
-            if (wbase + lane + u * kThreads < nruns)
-                load_act_run<R, MODE>(p, ch0, runs_per_tok, wbase + lane + u * kThreads, v[u], isum[u]);
+            if (mylane < rpw && wbase + mylane + u * rstep < nruns)
+                load_act_run<R, MODE>(p, ch0, runs_per_tok, wbase + mylane + u * rstep, v[u], isum[u]);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int idx = wbase + lane + u * kThreads;
-            const bool valid = idx < nruns;   // whole quads: nruns is a multiple of 4
+            const int idx = wbase + mylane + u * rstep;
+            const bool valid = mylane < rpw && idx < nruns;   // whole quads: nruns % 4 == 0
             float sum = 0.f, csum = 0.f;
             int m = 0, lc = 0, gi = 0, tt = 0;
             if (valid) {
@@ -356,15 +362,15 @@ __device__ __forceinline__ void stage_activations(const GemvParams &p, uint16_t 
                     *reinterpret_cast<uint4 *>(dst + 8 * ((j >> 1) ^ swz)) = o;
                 }
             }
-            const float s1 = __shfl_down_sync(0xffffffffu, sum, 1);
-            const float s2 = __shfl_down_sync(0xffffffffu, sum, 2);
-            const float s3 = __shfl_down_sync(0xffffffffu, sum, 3);
+            const float s1 = __shfl_down_sync(0xffffffffu, sum, 1 * sp);
+            const float s2 = __shfl_down_sync(0xffffffffu, sum, 2 * sp);
+            const float s3 = __shfl_down_sync(0xffffffffu, sum, 3 * sp);
             if (valid && tt == 0)
                 xs[(lc * NGC + gi) * MP + m] = ((sum + s1) + s2) + s3;
             if constexpr (MODE == 0) {
-                const float c1 = __shfl_down_sync(0xffffffffu, csum, 1);
-                const float c2 = __shfl_down_sync(0xffffffffu, csum, 2);
-                const float c3 = __shfl_down_sync(0xffffffffu, csum, 3);
+                const float c1 = __shfl_down_sync(0xffffffffu, csum, 1 * sp);
+                const float c2 = __shfl_down_sync(0xffffffffu, csum, 2 * sp);
+                const float c3 = __shfl_down_sync(0xffffffffu, csum, 3 * sp);
                 if (valid && tt == 0)
                     cs[(lc * NGC + gi) * MP + m] = ((csum + c1) + c2) + c3;
             }
