@@ -29,6 +29,7 @@ import ctypes
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -49,10 +50,15 @@ KERNEL_SOURCES = ["skinny.cuh", "gemv.cu", "gemv.h", "common.cuh", "unpack_plans
 
 
 def kernel_source_digest() -> str:
+    """Digest of the decode kernel's sources with comments and whitespace removed,
+    so that the recorded ncu traffic stays valid across comment-only edits."""
     h = hashlib.sha1()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "bit_weight_quantized_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "bit_weight_quantized_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:12]
 
 

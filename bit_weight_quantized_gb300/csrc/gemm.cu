@@ -8,15 +8,16 @@
 // memory and feeds tcgen05 MMAs that accumulate in tensor memory (TMEM).
 //
 // Tiles.  A CTA owns kBN = 192 weight columns (the MMA's N; 150 tiles cover
-// N = 28672 in one wave on 152 SMs) and walks the tokens in passes of two
-// 128-token M tiles, one TMEM accumulator each (2 x 192 of the 512 columns).
-// Per 64-wide K step: the x tiles (A operand, K-major, 128-byte swizzle) and,
-// every four K steps, a 192 x 256-code packed-weight tile arrive by TMA; twelve
-// dequant warps (two threads per weight column) turn 64 codes into bf16/fp16
-// (q - z) * s and write them in the same canonical K-major swizzled layout (B
-// operand); one thread issues 4 x 2 MMAs of K = 16; four epilogue warps move
-// the accumulators TMEM -> registers -> global memory.  The roles meet on
-// mbarriers; every wait is bounded and reports QMM_ERR_TIMEOUT.
+// N = 28672 in one wave on 152 SMs) and walks the tokens in passes of MT
+// 128-token M tiles, one TMEM accumulator each (MT = 2 for M > 128, MT = 1 with
+// a deeper pipeline for M <= 128).  Per 64-wide K step: the x tiles (A operand,
+// K-major, 128-byte swizzle) and, every four K steps, a 192 x 256-code
+// packed-weight tile arrive by TMA; twelve dequant warps (two threads per
+// weight column) turn 64 codes into bf16/fp16 (q - z) * s and write them in the
+// same canonical K-major swizzled layout (B operand); one thread issues
+// 4 x MT MMAs of K = 16; four epilogue warps move the accumulators TMEM ->
+// registers -> global memory.  The roles meet on mbarriers; every wait is
+// bounded and reports QMM_ERR_TIMEOUT.
 #include <cstring>
 
 #include "common.cuh"

@@ -39,9 +39,13 @@
 // codes of one group, so every MMA stays inside a group and the group's scale
 // is applied in fp32.  Codes become fp16 in registers with no shared-memory
 // round trip: a LOP3 keeps one code in each half of a 32-bit window and sets the
-// half's exponent so that it reads 2^E + q exactly; an exact HSUB2 removes 2^E.
-// Activations are staged once per CTA (or once per K phase when M x K does not
-// fit) in "slot" order -- the order in which codes come out of the registers.
+// half's exponent so that it reads 2^E + q exactly.  The fp16 path keeps 2^E in
+// the MMA operand and subtracts C[m][g] = sum_k 2^E_k x[m][k], formed exactly
+// by the activation staging, from each group's dot product in fp32; the W4A8
+// path removes 2^E with an exact HSUB2 so that its sums stay integers below
+// 2^24.  Activations are staged once per CTA (or once per K phase when M x K
+// does not fit) in "slot" order -- the order in which codes come out of the
+// registers -- with 16-byte chunks XOR-swizzled against bank conflicts.
 #pragma once
 
 #include <cuda.h>
