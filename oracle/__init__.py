@@ -14,7 +14,8 @@ arrays.  Citations for each step are in the C file's header:
 * dequantize ``w = s * (q - z)`` per group -- BitLLM Eq. (5), sec. 2.2;
 * fp64 matmul ``y = x . W^T``;
 * W4A8 integer core ``r + sum a_i b_i`` per group and fp64 epilogue --
-  BitLLM sec. 4.3 (dp4a), sec. 4.4 (deferred dequantization, Fig. 9).
+  BitLLM sec. 4.3 (dp4a), sec. 4.4 (deferred dequantization, Fig. 9);
+* per-token int8 quantization of fp16 activations -- BitLLM sec. 2.2 Eq. (1).
 
 Every function here is pinned by a ``-m "not gpu"`` test (hand-packed
 examples, round trips, brute force with Python integers/fractions, closed
@@ -43,7 +44,7 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".{os.getpid()}.tmp"
         subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
-                               "-Wall", "-Wextra", "-o", tmp, _SRC])
+                               "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -70,6 +71,8 @@ def _load():
             lib.oracle_w4a8.restype = I
             lib.oracle_threads.argtypes = [I, L]
             lib.oracle_threads.restype = I
+            lib.oracle_quantize_act.argtypes = [P, P, P, L, L]
+            lib.oracle_quantize_act.restype = None
             _lib = lib
     return _lib
 
@@ -190,3 +193,14 @@ def solve_w4a8(prob, rows=None, cols=None, want_acc=True, nthreads: int = 0):
     sa = prob.sa.astype(np.float64) if rows is None else prob.sa.astype(np.float64)[rows]
     ws = prob.ws.astype(np.float64) if cols is None else prob.ws.astype(np.float64)[cols]
     return w4a8(xq, sa, packed, ws, prob.group, prob.K, want_acc, nthreads)
+
+
+def quantize_act(x_bits: np.ndarray):
+    """Per-token int8 quantization of fp16 activations given as bit patterns
+    (uint16 [M][K]); returns (xq int8 [M][K], sa fp16 bit patterns uint16 [M])."""
+    x = _c(x_bits, np.uint16)
+    M, K = x.shape
+    xq = np.zeros((M, K), dtype=np.int8)
+    sa = np.zeros(M, dtype=np.uint16)
+    _load().oracle_quantize_act(_ptr(x), _ptr(xq), _ptr(sa), M, K)
+    return xq, sa

@@ -25,10 +25,18 @@
  *     activations; the integer core is the dp4a identity
  *     r + sum_i a_i*b_i accumulated per group of G into an integer; the
  *     epilogue is y = sa[m] * sum_g ws[n][g] * acc[m][n][g] in fp64.
+ *  5. Per-token int8 quantization of fp16 activations (BitLLM sec. 2.2,
+ *     Eq. (1), q = clip(round(x/s) + z, q_min, q_max), with the int8 range
+ *     of Fig. 2(a)).  Reading: symmetric per token (z = 0), s = the token's
+ *     largest |x| divided by 127 and stored as fp16, rounding half to even,
+ *     q = 0 for a token whose stored scale is 0.  The quotients that decide
+ *     the integers are single-precision IEEE divisions (the precision the
+ *     GPU kernel uses too).
  *
  * Every function follows the definition directly: per-bit loops, no word
  * tricks, no blocking.
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -219,4 +227,48 @@ int oracle_w4a8(const int8_t *xq, const double *sa, const uint8_t *w4,
     w4a8_ctx c = { xq, sa, w4, ws, group, acc, y, M, N, K, 0 };
     parallel_columns(w4a8_cols, &c, N, nthreads);
     return c.overflow;
+}
+
+/* ---- 5. per-token int8 activation quantization ------------------------- */
+
+static float f16_bits_to_float(uint16_t h)
+{
+    _Float16 v;
+    memcpy(&v, &h, sizeof(v));
+    return (float)v;   /* exact */
+}
+
+static uint16_t float_to_f16_bits(float f)
+{
+    _Float16 v = (_Float16)f;   /* round to nearest even */
+    uint16_t h;
+    memcpy(&h, &v, sizeof(h));
+    return h;
+}
+
+/* x: fp16 bit patterns [M][K]; writes xq int8 [M][K] and sa fp16 bits [M]. */
+void oracle_quantize_act(const uint16_t *x, int8_t *xq, uint16_t *sa, long M, long K)
+{
+    for (long m = 0; m < M; ++m) {
+        const uint16_t *row = x + m * K;
+        float amax = 0.0f;
+        for (long k = 0; k < K; ++k) {
+            const float a = fabsf(f16_bits_to_float(row[k]));
+            if (a > amax)
+                amax = a;
+        }
+        sa[m] = float_to_f16_bits(amax / 127.0f);
+        const float s = f16_bits_to_float(sa[m]);
+        for (long k = 0; k < K; ++k) {
+            float q = 0.0f;
+            if (s > 0.0f) {
+                q = rintf(f16_bits_to_float(row[k]) / s);   /* ties to even */
+                if (q < -128.0f)
+                    q = -128.0f;
+                if (q > 127.0f)
+                    q = 127.0f;
+            }
+            xq[m * K + k] = (int8_t)q;
+        }
+    }
 }

@@ -252,3 +252,43 @@ def test_w4a8_extreme_accumulator_fits_int32():
     assert not ov
     assert (acc == 127 * 8 * G).all()
     assert y[0, 0] == 2 * 127 * 8 * G
+
+
+# ---- per-token int8 activation quantization (BitLLM sec. 2.2, Eq. (1)) -------------------
+@pytest.mark.parametrize("case", list(_golden_lines("act_quant_examples.txt")))
+def test_act_quant_worked_examples(case):
+    xs, s, qs = (part.split() for part in case)
+    x = np.array([float(v) for v in xs], dtype=np.float16).reshape(1, -1)
+    q, sa = oracle.quantize_act(x.view(np.uint16))
+    assert float(sa.view(np.float16)[0]) == float(s[0])
+    assert q[0].tolist() == [int(v) for v in qs]
+
+
+def test_act_quant_matches_ieee_single_precision():
+    # the scale and the quotients are IEEE single-precision divisions rounded to
+    # fp16 / to the nearest integer (ties to even): numpy's float32 arithmetic
+    # and rint implement the same IEEE operations independently of the C code
+    rng = np.random.default_rng(7)
+    rows = [rng.standard_normal(512) * m for m in (1e-6, 3e-3, 1.0, 40.0, 1e4)]
+    rows.append(np.where(rng.random(512) < 0.5, 0.5, -0.5) * 127.0 / 64.0)   # exact ties
+    x = np.array(rows, dtype=np.float16)
+    q, sa = oracle.quantize_act(x.view(np.uint16))
+    x32 = x.astype(np.float32)
+    amax = np.max(np.abs(x32), axis=1)
+    s_ref = (amax / np.float32(127)).astype(np.float16)
+    np.testing.assert_array_equal(sa, s_ref.view(np.uint16))
+    s32 = s_ref.astype(np.float32)[:, None]
+    q_ref = np.where(s32 > 0, np.clip(np.rint(x32 / np.where(s32 > 0, s32, 1)), -128, 127), 0)
+    np.testing.assert_array_equal(q, q_ref.astype(np.int8))
+
+
+def test_act_quant_error_bound_and_range():
+    # |x - s q| <= s / 2 (round to nearest, no clipping since |x| / s <= 127 up to
+    # the scale's fp16 rounding), and |q| <= 127
+    rng = np.random.default_rng(11)
+    x = np.array(rng.standard_normal((8, 1024)) * rng.uniform(0.01, 100, (8, 1)), dtype=np.float16)
+    q, sa = oracle.quantize_act(x.view(np.uint16))
+    s = sa.view(np.float16).astype(np.float64)[:, None]
+    err = np.abs(x.astype(np.float64) - s * q.astype(np.float64))
+    assert np.all(err <= s / 2 * (1 + 1e-6))
+    assert np.abs(q.astype(np.int32)).max() <= 127
