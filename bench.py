@@ -289,8 +289,9 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf):
     """The other workload families, timed the same way on device-generated
     inputs of the workloads' shapes and laws (the values do not change the
     work): skinny decode (M = 16, N = 14336, b = 6, group 64), the tiled path
-    (M = 128 / 512 / 2048, K = 8192, N = 28672, int4, bf16) and W4A8
-    (M = 1 / 16 / 64, K = N = 4096)."""
+    (M = 128 / 512 / 2048, K = 8192, N = 28672, int4, bf16), W4A8
+    (M = 1 / 16 / 64, K = N = 4096; also fed from fp16 activations through the
+    per-token int8 quantizer) and the quantizer alone (K = 4096)."""
     out = {}
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
@@ -335,6 +336,27 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf):
         out[f"w4a8_M{M}"] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
                              "frac_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4),
                              "TOPs": round(2.0 * M * N * K / ms / 1e9, 1)}
+        # the same from fp16 activations: per-token int8 quantizer + W4A8
+        x16 = torch.randn(M, K, device=dev, generator=gen).half()
+        xq_b = torch.empty(M, K, dtype=torch.int8, device=dev)
+        sa_b = torch.empty(M, dtype=torch.float16, device=dev)
+
+        def chain(w, x16=x16, xq_b=xq_b, sa_b=sa_b, y=y):
+            q.qmm_quantize_act(x16, xq_b, sa_b)
+            q.qmm_w4a8(xq_b, sa_b, w[0], w[1], 128, out=y)
+        ms = time_graph(torch, stream, [lambda w=w_: chain(w) for w_ in wsets])
+        out[f"w4a8_fp16_in_M{M}"] = {"us": round(ms * 1e3, 2), "note": "qmm_quantize_act + qmm_w4a8"}
+    del wsets
+    # per-token int8 activation quantizer alone: K = 4096, inputs rotate over 8 copies
+    K = 4096
+    for M in (1, 64, 2048):
+        xs = [torch.randn(M, K, device=dev, generator=gen).half() for _ in range(8)]
+        xq_b = torch.empty(M, K, dtype=torch.int8, device=dev)
+        sa_b = torch.empty(M, dtype=torch.float16, device=dev)
+        ms = time_graph(torch, stream, [lambda x=x_: q.qmm_quantize_act(x, xq_b, sa_b) for x_ in xs])
+        nbytes = M * K * 2 + M * K + M * 2
+        out[f"quantize_act_M{M}"] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
+                                     "frac_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4)}
     return out
 
 # ---- GPU leg -------------------------------------------------------------------------------

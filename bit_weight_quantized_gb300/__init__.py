@@ -39,6 +39,7 @@ SIGNATURES = {
     "qmm_gemv": ([_P, _I, _P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P], _I),
     "qmm_gemm": ([_P, _I, _P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P], _I),
     "qmm_w4a8": ([_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P], _I),
+    "qmm_quantize_act": ([_P, _P, _P, _I, _I, _P], _I),
     "qmm_device_status": ([_P], _I),
     "qmm_watchdog_selftest": ([_P], _I),
     "qmm_status_string": ([_I], ctypes.c_char_p),
@@ -185,6 +186,23 @@ def qmm_w4a8(xq, sa, w4, ws, group=128, want_acc=False, out=None, acc_out=None):
     _check(load().qmm_w4a8(_ptr(xq), _ptr(sa), _ptr(w4), _ptr(ws), group, _ptr(out),
                            _ptr(acc_out), M, N, K, _stream(xq.device)), "qmm_w4a8")
     return (out, acc_out) if want_acc else out
+
+
+def qmm_quantize_act(x, xq=None, sa=None):
+    """Per-token int8 quantization of fp16 activations for qmm_w4a8: returns
+    (xq int8 [M][K], sa fp16 [M]) with sa = fp16(max|x| / 127) and
+    xq = round-half-even(x / sa) clipped to [-128, 127]."""
+    _dev(x, "x", torch.float16)
+    M, K = x.shape
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if sa is None:
+        sa = torch.empty((M,), dtype=torch.float16, device=x.device)
+    _dev(xq, "xq", torch.int8, (M, K))
+    _dev(sa, "sa", torch.float16, (M,))
+    _check(load().qmm_quantize_act(_ptr(x), _ptr(xq), _ptr(sa), M, K, _stream(x.device)),
+           "qmm_quantize_act")
+    return xq, sa
 
 
 def qmm_device_status(stream=None) -> int:

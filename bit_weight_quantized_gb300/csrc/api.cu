@@ -334,6 +334,25 @@ qmm_status qmm_w4a8(const int8_t *xq, const void *sa, const uint8_t *w4, const v
                          f->smem_optin, f->smem_pair, stream);
 }
 
+qmm_status qmm_quantize_act(const void *x, int8_t *xq, void *sa, int M, int K, cudaStream_t stream)
+{
+    if (M < 0 || K < 0 || K % 8)
+        return QMM_ERR_SHAPE;
+    if (M == 0)
+        return QMM_OK;
+    if (!sa || (K > 0 && (!x || !xq)))
+        return QMM_ERR_NULL;
+    if (!aligned(sa, 2) || (K > 0 && (!aligned(x, 16) || !aligned(xq, 16))))
+        return QMM_ERR_ALIGN;
+    const DeviceFacts *f = device_facts();
+    if (!f || f->usable != QMM_OK)
+        return QMM_ERR_DEVICE;
+    if (K == 0)   // max over an empty row is 0: every scale is 0
+        return from_cuda(cudaMemsetAsync(sa, 0, static_cast<size_t>(M) * 2, stream));
+    return from_cuda(launch_quantize_act(static_cast<const uint16_t *>(x), xq, static_cast<uint16_t *>(sa),
+                                         M, K, stream));
+}
+
 qmm_status qmm_watchdog_selftest(cudaStream_t stream)
 {
     const DeviceFacts *f = device_facts();

@@ -58,6 +58,9 @@ cudaError_t gemv_launch_w7(const GemvParams &, int, int, cudaStream_t);
 cudaError_t gemv_launch_w8(const GemvParams &, int, int, cudaStream_t);
 cudaError_t w4a8_launch(const GemvParams &, int, int, cudaStream_t);
 
+// quant.cu: per-token int8 quantization of fp16 activations (one CTA per token).
+cudaError_t launch_quantize_act(const uint16_t *x, int8_t *xq, uint16_t *sa, int M, int K,
+                                cudaStream_t stream);
 cudaError_t launch_pack(const uint8_t *codes, uint8_t *packed, int N, int K, int bits,
                         int32_t *bad_count, cudaStream_t stream, int num_sms);
 cudaError_t launch_unpack(const uint8_t *packed, uint8_t *codes, int N, int K, int bits,

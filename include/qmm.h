@@ -141,6 +141,28 @@ QMM_API qmm_status qmm_w4a8(const int8_t *xq, const void *sa, const uint8_t *w4,
                     int group, void *y, int32_t *acc_out, int M, int N, int K,
                     cudaStream_t stream);
 
+/* Per-token int8 quantization of fp16 activations, the step before qmm_w4a8
+ * (BitLLM sec. 2.2, Eq. (1): q = clip(round(x / s) + z, q_min, q_max), with
+ * the int8 range of Fig. 2(a)).  Reading of the pages (which do not fix how s
+ * is chosen): symmetric per token, z = 0,
+ *   sa[m]    = fp16( max_k |x[m][k]| / 127 )  -- IEEE single-precision
+ *              division, then rounded to the nearest fp16 (ties to even);
+ *   xq[m][k] = clip( round( x[m][k] / sa[m] ), -128, 127 )  -- IEEE
+ *              single-precision division, rounded to the nearest integer
+ *              (ties to even); xq = 0 for a token with sa[m] == 0.
+ * The result is exact and reproducible: every integer is decided by the same
+ * IEEE operations.  x must be finite.
+ *   x    (device) fp16 [M][K], 16-byte aligned.
+ *   xq   (device) int8 [M][K], 16-byte aligned, fully overwritten.
+ *   sa   (device) fp16 [M], 2-byte aligned, fully overwritten (all 0 if K == 0).
+ *   K % 8 == 0.  One CTA per token; like the matmul calls it launches with
+ *   programmatic dependent launch and reads x only after waiting for the
+ *   preceding kernel on the stream.
+ * Errors: QMM_ERR_SHAPE (M or K negative, K % 8), QMM_ERR_NULL, QMM_ERR_ALIGN,
+ * QMM_ERR_DEVICE, QMM_ERR_CUDA; nothing is launched on an argument error. */
+QMM_API qmm_status qmm_quantize_act(const void *x, int8_t *xq, void *sa, int M, int K,
+                                    cudaStream_t stream);
+
 /* Synchronizes `stream`, then returns and clears the first device-side error
  * recorded by any qmm kernel on the current device (QMM_OK if none).  A
  * pending asynchronous CUDA error is reported as QMM_ERR_CUDA. */

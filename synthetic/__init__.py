@@ -238,3 +238,11 @@ def tiled(M: int, seed: int = 0) -> QmmProblem:
 def w4a8(M: int, seed: int = 0) -> W4A8Problem:
     """M in {1,16,64}, K=N=4096, group 128."""
     return make_w4a8(M, 4096, 4096, 128, seed=seed, label=f"w4a8_M{M}")
+
+
+def make_act(M: int, K: int, seed: int = 0) -> np.ndarray:
+    """fp16 activations [M][K] for the per-token int8 quantizer: N(0,1) times a
+    per-token magnitude 10**u, u uniform in [-2, 2) (from the same stream)."""
+    st = SplitMix64(seed)
+    mag = 10.0 ** (4.0 * (st.next(M) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53) - 2.0)
+    return (st.normal(M * K).reshape(M, K) * mag[:, None]).astype(np.float16)

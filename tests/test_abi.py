@@ -92,6 +92,16 @@ def test_gemm_and_w4a8_argument_errors(lib):
     assert lib.qmm_w4a8(_fake(0x10004), A16, B16, A16, 128, B16, None, 1, 64, 128, None) == 4
 
 
+def test_quantize_act_argument_errors(lib):
+    assert lib.qmm_quantize_act(A16, B16, A16, 2, 12, None) == 3            # K % 8
+    assert lib.qmm_quantize_act(A16, B16, A16, -1, 64, None) == 3
+    assert lib.qmm_quantize_act(None, B16, A16, 2, 64, None) == 1
+    assert lib.qmm_quantize_act(A16, B16, None, 2, 64, None) == 1
+    assert lib.qmm_quantize_act(_fake(0x10008), B16, A16, 2, 64, None) == 4  # x 16-byte aligned
+    assert lib.qmm_quantize_act(A16, B16, _fake(0x10001), 2, 64, None) == 4
+    assert lib.qmm_quantize_act(None, None, None, 0, 64, None) == 0          # no tokens
+
+
 def test_pack_argument_errors(lib):
     assert lib.qmm_pack(A16, B16, 4, 3, 3, None, None) == 3   # K*bits not byte aligned
     assert lib.qmm_pack(A16, B16, 4, 8, 0, None, None) == 2
