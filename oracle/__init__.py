@@ -14,7 +14,8 @@ arrays.  Citations for each step are in the C file's header:
 * dequantize ``w = s * (q - z)`` per group -- BitLLM Eq. (5), sec. 2.2;
 * fp64 matmul ``y = x . W^T``;
 * W4A8 integer core ``r + sum a_i b_i`` per group and fp64 epilogue --
-  BitLLM sec. 4.3 (dp4a), sec. 4.4 (deferred dequantization, Fig. 9);
+  BitLLM sec. 4.3 (dp4a), sec. 4.4 (deferred dequantization, Fig. 9); the
+  same core with signed 8-bit weights is W8A8 (BitLLM, Experiment Setup);
 * per-token int8 quantization of fp16 activations -- BitLLM sec. 2.2 Eq. (1).
 
 Every function here is pinned by a ``-m "not gpu"`` test (hand-packed
@@ -69,6 +70,10 @@ def _load():
             lib.oracle_dot_i8.restype = ctypes.c_int64
             lib.oracle_w4a8.argtypes = [P, P, P, P, I, P, P, L, L, L, I]
             lib.oracle_w4a8.restype = I
+            lib.oracle_wxa8.argtypes = [P, P, P, I, P, I, P, P, L, L, L, I]
+            lib.oracle_wxa8.restype = I
+            lib.oracle_signed_value.argtypes = [I, I]
+            lib.oracle_signed_value.restype = I
             lib.oracle_threads.argtypes = [I, L]
             lib.oracle_threads.restype = I
             lib.oracle_quantize_act.argtypes = [P, P, P, L, L]
@@ -144,6 +149,10 @@ def int4_value(code: int) -> int:
     return int(_load().oracle_int4_value(code))
 
 
+def signed_value(code: int, bits: int) -> int:
+    return _load().oracle_signed_value(int(code), bits)
+
+
 def dot_i8(a: np.ndarray, b: np.ndarray, r: int = 0) -> int:
     a = _c(a, np.int8)
     b = _c(b, np.int8)
@@ -204,3 +213,29 @@ def quantize_act(x_bits: np.ndarray):
     sa = np.zeros(M, dtype=np.uint16)
     _load().oracle_quantize_act(_ptr(x), _ptr(xq), _ptr(sa), M, K)
     return xq, sa
+
+
+def wxa8(xq: np.ndarray, sa_f64: np.ndarray, w_packed: np.ndarray, bits: int, ws_f64: np.ndarray,
+         group: int, K: int, want_acc: bool = True, nthreads: int = 0):
+    """Signed b-bit weights x int8 activations (b = 4: W4A8, b = 8: W8A8).
+    Returns (y fp64 [M][N], acc int64 [M][N][K/group] or None, overflow flag)."""
+    xq = _c(xq, np.int8)
+    sa = _c(sa_f64, np.float64)
+    w = _c(w_packed, np.uint8)
+    ws = _c(ws_f64, np.float64)
+    M = xq.shape[0]
+    N = w.shape[0]
+    if xq.shape[1] != K or w.shape[1] * 8 != K * bits or K % group or ws.shape != (N, K // group):
+        raise ValueError("shape mismatch")
+    y = np.empty((M, N), dtype=np.float64)
+    acc = np.empty((M, N, K // group), dtype=np.int64) if want_acc else None
+    ov = _load().oracle_wxa8(_ptr(xq), _ptr(sa), _ptr(w), bits, _ptr(ws), group,
+                             None if acc is None else _ptr(acc), _ptr(y), M, N, K, nthreads)
+    return y, acc, bool(ov)
+
+
+def solve_w8a8(prob, want_acc=True, nthreads: int = 0):
+    """A synthetic.W8A8Problem: the weights are int8 values stored as bytes."""
+    w = np.ascontiguousarray(prob.w8.view(np.uint8))
+    return wxa8(prob.xq, prob.sa.astype(np.float64), w, 8, prob.ws.astype(np.float64),
+                prob.group, prob.K, want_acc, nthreads)

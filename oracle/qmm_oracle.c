@@ -24,7 +24,9 @@
  *     nibbles, even k in the low nibble, no zero point) and int8
  *     activations; the integer core is the dp4a identity
  *     r + sum_i a_i*b_i accumulated per group of G into an integer; the
- *     epilogue is y = sa[m] * sum_g ws[n][g] * acc[m][n][g] in fp64.
+ *     epilogue is y = sa[m] * sum_g ws[n][g] * acc[m][n][g] in fp64.  The
+ *     same core with signed 8-bit weights (two's-complement bytes) is the
+ *     W8A8 precision BitLLM evaluates beside W4A8 (Experiment Setup).
  *  5. Per-token int8 quantization of fp16 activations (BitLLM sec. 2.2,
  *     Eq. (1), q = clip(round(x/s) + z, q_min, q_max), with the int8 range
  *     of Fig. 2(a)).  Reading: symmetric per token (z = 0), s = the token's
@@ -179,6 +181,14 @@ int oracle_int4_value(int code)
     return (code & 8) ? (code & 15) - 16 : (code & 15);
 }
 
+/* Value of a b-bit two's-complement code: the top bit weighs -2^(b-1). */
+int oracle_signed_value(int code, int bits)
+{
+    const int top = 1 << (bits - 1);
+    code &= (1 << bits) - 1;
+    return (code & top) ? code - 2 * top : code;
+}
+
 /* The dot-product primitive: r + sum_i a[i]*b[i] with int8 inputs and a wide
  * integer accumulator (dp4a is the n = 4 case). */
 int64_t oracle_dot_i8(const int8_t *a, const int8_t *b, long n, int64_t r)
@@ -190,18 +200,18 @@ int64_t oracle_dot_i8(const int8_t *a, const int8_t *b, long n, int64_t r)
 
 typedef struct {
     const int8_t *xq; const double *sa; const uint8_t *w4; const double *ws;
-    int group; int64_t *acc; double *y; long M, N, K; int overflow;
+    int group; int64_t *acc; double *y; long M, N, K; int overflow; int bits;
 } w4a8_ctx;
 
 static void w4a8_cols(void *p, long n0, long n1)
 {
     w4a8_ctx *c = (w4a8_ctx *)p;
-    long K = c->K, ng = K / c->group, row_bytes = K / 2;
+    long K = c->K, ng = K / c->group, row_bytes = K * c->bits / 8;
     int8_t *w = (int8_t *)malloc((size_t)(K > 0 ? K : 1));
     for (long n = n0; n < n1; ++n) {
         const uint8_t *row = c->w4 + n * row_bytes;
         for (long k = 0; k < K; ++k)
-            w[k] = (int8_t)oracle_int4_value(oracle_code(row, k, 4));
+            w[k] = (int8_t)oracle_signed_value(oracle_code(row, k, c->bits), c->bits);
         for (long m = 0; m < c->M; ++m) {
             double yy = 0.0;
             for (long g = 0; g < ng; ++g) {
@@ -224,7 +234,20 @@ int oracle_w4a8(const int8_t *xq, const double *sa, const uint8_t *w4,
                 const double *ws, int group, int64_t *acc, double *y,
                 long M, long N, long K, int nthreads)
 {
-    w4a8_ctx c = { xq, sa, w4, ws, group, acc, y, M, N, K, 0 };
+    w4a8_ctx c = { xq, sa, w4, ws, group, acc, y, M, N, K, 0, 4 };
+    parallel_columns(w4a8_cols, &c, N, nthreads);
+    return c.overflow;
+}
+
+/* The same with signed b-bit weights (b = 8: W8A8, BitLLM's other integer
+ * precision, Experiment Setup "Workloads": 8-bit weights and activations with
+ * group-wise scaling): w[n][k] is the two's-complement value of code k of
+ * column n's b-bit stream. */
+int oracle_wxa8(const int8_t *xq, const double *sa, const uint8_t *w, int bits,
+                const double *ws, int group, int64_t *acc, double *y,
+                long M, long N, long K, int nthreads)
+{
+    w4a8_ctx c = { xq, sa, w, ws, group, acc, y, M, N, K, 0, bits };
     parallel_columns(w4a8_cols, &c, N, nthreads);
     return c.overflow;
 }

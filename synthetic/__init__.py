@@ -246,3 +246,31 @@ def make_act(M: int, K: int, seed: int = 0) -> np.ndarray:
     st = SplitMix64(seed)
     mag = 10.0 ** (4.0 * (st.next(M) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53) - 2.0)
     return (st.normal(M * K).reshape(M, K) * mag[:, None]).astype(np.float16)
+
+
+@dataclass
+class W8A8Problem:
+    """Integer-native W8A8: int8 weights and activations, per-group weight
+    scales and per-token activation scales."""
+    M: int
+    N: int
+    K: int
+    group: int
+    w8: np.ndarray   # int8 [N][K]
+    ws: np.ndarray   # fp16 [N][K/group]
+    xq: np.ndarray   # int8 [M][K]
+    sa: np.ndarray   # fp16 [M]
+    label: str = ""
+
+    def algorithmic_bytes(self) -> int:
+        return self.N * self.K + self.ws.size * 2 + self.M * self.K + self.M * 2 + self.M * self.N * 2
+
+
+def make_w8a8(M: int, N: int, K: int, group: int = 32, seed: int = 0, label: str = "") -> W8A8Problem:
+    """w ~ U[-128, 127] (all 256 byte values), xq ~ U[-127, 127], ws and sa by the scale law."""
+    st = SplitMix64(seed)
+    w8 = st.uniform_bits(N * K, 8).astype(np.uint8).view(np.int8).reshape(N, K)
+    ws = scale_law(st, N * (K // group)).reshape(N, K // group)
+    xq = st.uniform_int8_sym(M * K).reshape(M, K)
+    sa = scale_law(st, M)
+    return W8A8Problem(M, N, K, group, w8, ws, xq, sa, label)

@@ -14,6 +14,7 @@ import numpy as np
 import pytest
 
 import oracle
+import synthetic
 from synthetic import SplitMix64
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -292,3 +293,45 @@ def test_act_quant_error_bound_and_range():
     err = np.abs(x.astype(np.float64) - s * q.astype(np.float64))
     assert np.all(err <= s / 2 * (1 + 1e-6))
     assert np.abs(q.astype(np.int32)).max() <= 127
+
+
+# ---- W8A8: signed 8-bit weights (BitLLM, Experiment Setup) ------------------------------
+def test_signed_value_table():
+    assert [oracle.signed_value(c, 8) for c in (0, 1, 127, 128, 129, 255)] == [0, 1, 127, -128, -127, -1]
+    assert [oracle.signed_value(c, 4) for c in (0, 7, 8, 9, 15)] == [0, 7, -8, -7, -1]
+    assert [oracle.signed_value(c, 4) for c in range(16)] == [oracle.int4_value(c) for c in range(16)]
+
+
+def test_w8a8_brute_force_exact():
+    prob = synthetic.make_w8a8(3, 5, 96, 32, seed=3)
+    y, acc, ov = oracle.solve_w8a8(prob)
+    assert not ov
+    ng = prob.K // prob.group
+    for m in range(prob.M):
+        for n in range(prob.N):
+            yy = 0.0
+            for g in range(ng):
+                ks = range(g * prob.group, (g + 1) * prob.group)
+                a = sum(int(prob.xq[m, k]) * int(prob.w8[n, k]) for k in ks)   # Python integers
+                assert acc[m, n, g] == a
+                yy += float(prob.ws[n, g]) * a
+            assert y[m, n] == float(prob.sa[m]) * yy
+
+
+def test_w8a8_extreme_accumulator():
+    prob = synthetic.make_w8a8(2, 3, 256, 128, seed=4)
+    prob.w8[:] = -128
+    prob.xq[:] = -127
+    _, acc, ov = oracle.solve_w8a8(prob)
+    assert not ov and (acc == 128 * 127 * 128).all()
+
+
+def test_wxa8_at_four_bits_is_w4a8():
+    prob = synthetic.make_w4a8(3, 7, 256, 64, seed=9)
+    packed, _ = oracle.pack(prob.w4, 4)
+    y4, acc4, _ = oracle.w4a8(prob.xq, prob.sa.astype(np.float64), packed, prob.ws.astype(np.float64),
+                              prob.group, prob.K)
+    yx, accx, _ = oracle.wxa8(prob.xq, prob.sa.astype(np.float64), packed, 4, prob.ws.astype(np.float64),
+                              prob.group, prob.K)
+    np.testing.assert_array_equal(acc4, accx)
+    np.testing.assert_array_equal(y4, yx)
