@@ -291,7 +291,8 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf):
     work): skinny decode (M = 16, N = 14336, b = 6, group 64), the tiled path
     (M = 128 / 512 / 2048, K = 8192, N = 28672, int4, bf16), W4A8
     (M = 1 / 16 / 64, K = N = 4096; also fed from fp16 activations through the
-    per-token int8 quantizer) and the quantizer alone (K = 4096)."""
+    per-token int8 quantizer), W8A8 (the same shapes, group 32) and the
+    quantizer alone (K = 4096)."""
     out = {}
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
@@ -346,6 +347,19 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf):
             q.qmm_w4a8(xq_b, sa_b, w[0], w[1], 128, out=y)
         ms = time_graph(torch, stream, [lambda w=w_: chain(w) for w_ in wsets])
         out[f"w4a8_fp16_in_M{M}"] = {"us": round(ms * 1e3, 2), "note": "qmm_quantize_act + qmm_w4a8"}
+    del wsets
+    # W8A8: K = N = 4096, int8 weights, group 32 (the pages' W8A8 setting)
+    wsets = [(torch.randint(-128, 128, (N, K), dtype=torch.int8, device=dev, generator=gen),
+              scales(N, K // 32)) for _ in range(8)]
+    for M in (1, 16, 64):
+        xq = torch.randint(-127, 128, (M, K), dtype=torch.int8, device=dev, generator=gen)
+        sa = (0.02 * torch.randn(M, device=dev, generator=gen).abs() + 1e-3).half()
+        y = torch.empty(M, N, dtype=torch.float16, device=dev)
+        ms = time_graph(torch, stream, [lambda w=w_: q.qmm_w8a8(xq, sa, w[0], w[1], 32, out=y) for w_ in wsets])
+        nbytes = N * K + N * (K // 32) * 2 + M * K + M * 2 + M * N * 2
+        out[f"w8a8_M{M}_g32"] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
+                                 "frac_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4),
+                                 "TOPs": round(2.0 * M * N * K / ms / 1e9, 1)}
     del wsets
     # per-token int8 activation quantizer alone: K = 4096, inputs rotate over 8 copies
     K = 4096

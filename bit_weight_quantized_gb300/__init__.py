@@ -39,6 +39,7 @@ SIGNATURES = {
     "qmm_gemv": ([_P, _I, _P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P], _I),
     "qmm_gemm": ([_P, _I, _P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P], _I),
     "qmm_w4a8": ([_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P], _I),
+    "qmm_w8a8": ([_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P], _I),
     "qmm_quantize_act": ([_P, _P, _P, _I, _I, _P], _I),
     "qmm_device_status": ([_P], _I),
     "qmm_watchdog_selftest": ([_P], _I),
@@ -185,6 +186,26 @@ def qmm_w4a8(xq, sa, w4, ws, group=128, want_acc=False, out=None, acc_out=None):
         acc_out = torch.empty((M, N, K // group), dtype=torch.int32, device=xq.device)
     _check(load().qmm_w4a8(_ptr(xq), _ptr(sa), _ptr(w4), _ptr(ws), group, _ptr(out),
                            _ptr(acc_out), M, N, K, _stream(xq.device)), "qmm_w4a8")
+    return (out, acc_out) if want_acc else out
+
+
+def qmm_w8a8(xq, sa, w8, ws, group=32, want_acc=False, out=None, acc_out=None):
+    """Integer-native W8A8 (int8 weights [N][K]): returns y (fp16 [M][N]) and, if
+    requested, the int32 accumulators [M][N][K/group]."""
+    _dev(xq, "xq", torch.int8)
+    M, K = xq.shape
+    _dev(sa, "sa", torch.float16, (M,))
+    _dev(w8, "w8", torch.int8)
+    N = w8.shape[0]
+    if w8.shape[1] != K:
+        raise ValueError("w8 must be [N][K]")
+    _dev(ws, "ws", torch.float16, (N, K // group))
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=xq.device)
+    if want_acc and acc_out is None:
+        acc_out = torch.empty((M, N, K // group), dtype=torch.int32, device=xq.device)
+    _check(load().qmm_w8a8(_ptr(xq), _ptr(sa), _ptr(w8), _ptr(ws), group, _ptr(out),
+                           _ptr(acc_out), M, N, K, _stream(xq.device)), "qmm_w8a8")
     return (out, acc_out) if want_acc else out
 
 

@@ -330,8 +330,36 @@ qmm_status qmm_w4a8(const int8_t *xq, const void *sa, const uint8_t *w4, const v
         cudaError_t e = cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * 2, stream);
         return from_cuda(e);
     }
-    return w4a8_dispatch(xq, sa, w4, ws, group, y, acc_out, M, N, K, f->status, f->num_sms,
+    return wxa8_dispatch(4, xq, sa, w4, ws, group, y, acc_out, M, N, K, f->status, f->num_sms,
                          f->smem_optin, f->smem_pair, stream);
+}
+
+qmm_status qmm_w8a8(const int8_t *xq, const void *sa, const int8_t *w8, const void *ws,
+                    int group, void *y, int32_t *acc_out, int M, int N, int K,
+                    cudaStream_t stream)
+{
+    if (M < 0 || N < 0 || K < 0)
+        return QMM_ERR_SHAPE;
+    if (group != 32 && group != 64 && group != 128)
+        return QMM_ERR_SHAPE;
+    if (K % group || M > 64)
+        return QMM_ERR_SHAPE;
+    if (M == 0 || N == 0)
+        return QMM_OK;
+    if (!y)
+        return QMM_ERR_NULL;
+    if (K > 0 && (!xq || !sa || !w8 || !ws))
+        return QMM_ERR_NULL;
+    if (!aligned(xq, 16) || !aligned(w8, 16) || !aligned(ws, 2) || !aligned(sa, 2) ||
+        !aligned(y, 2) || (acc_out && !aligned(acc_out, 4)))
+        return QMM_ERR_ALIGN;
+    const DeviceFacts *f = device_facts();
+    if (!f || f->usable != QMM_OK)
+        return QMM_ERR_DEVICE;
+    if (K == 0)
+        return from_cuda(cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * 2, stream));
+    return wxa8_dispatch(8, xq, sa, reinterpret_cast<const uint8_t *>(w8), ws, group, y, acc_out, M, N,
+                         K, f->status, f->num_sms, f->smem_optin, f->smem_pair, stream);
 }
 
 qmm_status qmm_quantize_act(const void *x, int8_t *xq, void *sa, int M, int K, cudaStream_t stream)

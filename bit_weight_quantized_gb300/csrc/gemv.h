@@ -57,6 +57,7 @@ cudaError_t gemv_launch_w6(const GemvParams &, int, int, cudaStream_t);
 cudaError_t gemv_launch_w7(const GemvParams &, int, int, cudaStream_t);
 cudaError_t gemv_launch_w8(const GemvParams &, int, int, cudaStream_t);
 cudaError_t w4a8_launch(const GemvParams &, int, int, cudaStream_t);
+cudaError_t w8a8_launch(const GemvParams &, int, int, cudaStream_t);
 
 // quant.cu: per-token int8 quantization of fp16 activations (one CTA per token).
 cudaError_t launch_quantize_act(const uint16_t *x, int8_t *xq, uint16_t *sa, int M, int K,

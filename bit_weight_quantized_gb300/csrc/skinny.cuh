@@ -143,8 +143,8 @@ __device__ __forceinline__ uint32_t lop3_and_xor(uint32_t a, uint32_t mask, uint
 // a[i] = fp16 pair of plan pair i.  With SUB the pair is (q_lo, q_hi), exact
 // small integers; without it (2^E_lo + q_lo, 2^E_hi + q_hi), also exact, and
 // the caller removes sum_k 2^E_k x_k from the dot product instead (one
-// instruction per pair fewer on the integer/half pipe).  With FLIP8 each 4-bit
-// field is XORed with 8 first (signed int4 -> c xor 8).
+// instruction per pair fewer on the integer/half pipe).  With FLIP8 each field's
+// top bit is flipped first (signed int4 -> c xor 8, signed int8 -> c xor 128).
 template <int B, int R, bool FLIP8, bool SUB>
 __device__ __forceinline__ void extract_run(const uint32_t (&w)[(R * B + 31) / 32],
                                             uint32_t (&a)[R / 2])
@@ -153,7 +153,8 @@ __device__ __forceinline__ void extract_run(const uint32_t (&w)[(R * B + 31) / 3
     if constexpr (B == 8) {
 #pragma unroll
         for (int i = 0; i < R / 2; ++i) {
-            const uint32_t v = prmt(w[i >> 1], 0x64646464u, (i & 1) ? 0x4342u : 0x4140u);
+            const uint32_t wb = FLIP8 ? (w[i >> 1] ^ 0x80808080u) : w[i >> 1];   // int8 -> c xor 128
+            const uint32_t v = prmt(wb, 0x64646464u, (i & 1) ? 0x4342u : 0x4140u);
             a[i] = SUB ? hsub2(v, 0x64006400u) : v;
         }
     } else {
@@ -707,9 +708,10 @@ skinny_kernel(const GemvParams p)
                                         tot[i][nt][2] = fmaf(-zs[i][1], xv[nt].x, fmaf(sc[i][1], dd[2], tot[i][nt][2]));
                                         tot[i][nt][3] = fmaf(-zs[i][1], xv[nt].y, fmaf(sc[i][1], dd[3], tot[i][nt][3]));
                                     } else {
-                                        // exact integers: d and 8 X are below 2^24
-                                        const float acc0 = dd[0] - 8.f * xv[nt].x, acc1 = dd[1] - 8.f * xv[nt].y;
-                                        const float acc2 = dd[2] - 8.f * xv[nt].x, acc3 = dd[3] - 8.f * xv[nt].y;
+                                        // exact integers: d and 2^(B-1) X are below 2^24
+                                        constexpr float kOff = static_cast<float>(1 << (B - 1));
+                                        const float acc0 = dd[0] - kOff * xv[nt].x, acc1 = dd[1] - kOff * xv[nt].y;
+                                        const float acc2 = dd[2] - kOff * xv[nt].x, acc3 = dd[3] - kOff * xv[nt].y;
                                         tot[i][nt][0] = fmaf(sc[i][0], acc0, tot[i][nt][0]);
                                         tot[i][nt][1] = fmaf(sc[i][0], acc1, tot[i][nt][1]);
                                         tot[i][nt][2] = fmaf(sc[i][1], acc2, tot[i][nt][2]);

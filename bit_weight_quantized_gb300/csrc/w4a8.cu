@@ -6,7 +6,8 @@
 // every product and partial sum is an integer below 2^24, so fp32 accumulation
 // is exact -- and acc = D - 8 * sum x, the exact int32 accumulator.  The
 // epilogue applies the per-group weight scale and per-token activation scale:
-// y = sa[m] * sum_g ws[n][g] * acc.
+// y = sa[m] * sum_g ws[n][g] * acc.  The host dispatch here also serves W8A8
+// (signed int8 weights, w8a8.cu).
 #include <cstring>
 
 #include "gemv.h"
@@ -20,7 +21,7 @@ cudaError_t w4a8_launch(const GemvParams &p, int grid, int smem, cudaStream_t st
     return launch_skinny_width<4, 1>(p, grid, smem, stream);
 }
 
-qmm_status w4a8_dispatch(const int8_t *xq, const void *sa, const uint8_t *w4, const void *ws,
+qmm_status wxa8_dispatch(int bits, const int8_t *xq, const void *sa, const uint8_t *w, const void *ws,
                          int group, void *y, int32_t *acc_out, int M, int N, int K, int *status,
                          int num_sms, int smem_optin, int smem_pair, cudaStream_t stream)
 {
@@ -29,13 +30,13 @@ qmm_status w4a8_dispatch(const int8_t *xq, const void *sa, const uint8_t *w4, co
     p.xq = xq;
     p.sa = static_cast<const uint16_t *>(sa);
     p.acc_out = acc_out;
-    p.packed = w4;
+    p.packed = w;
     p.scales = static_cast<const uint16_t *>(ws);
     p.zeros = nullptr;
-    p.zero_const = 8;
+    p.zero_const = 1 << (bits - 1);
     p.y = y;
     p.status = status;
-    p.row_bytes = static_cast<long long>(K) / 2;
+    p.row_bytes = static_cast<long long>(K) * bits / 8;
     p.M = M;
     p.N = N;
     p.K = K;
@@ -43,11 +44,12 @@ qmm_status w4a8_dispatch(const int8_t *xq, const void *sa, const uint8_t *w4, co
     p.ng = K / group;
     p.y_bf16 = 0;
     int grid = 0, smem = 0;
-    qmm_status st = skinny_plan(p, 4, num_sms, smem_optin, smem_pair, &grid, &smem);
+    qmm_status st = skinny_plan(p, bits, num_sms, smem_optin, smem_pair, &grid, &smem);
     if (st != QMM_OK)
         return st;
-    p.use_bulk = (reinterpret_cast<uintptr_t>(w4) % 16 == 0) && (p.row_bytes % 16 == 0);
-    return w4a8_launch(p, grid, smem, stream) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+    p.use_bulk = (reinterpret_cast<uintptr_t>(w) % 16 == 0) && (p.row_bytes % 16 == 0);
+    const cudaError_t e = bits == 8 ? w8a8_launch(p, grid, smem, stream) : w4a8_launch(p, grid, smem, stream);
+    return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
 }
 
 }  // namespace qmm

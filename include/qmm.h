@@ -141,6 +141,18 @@ QMM_API qmm_status qmm_w4a8(const int8_t *xq, const void *sa, const uint8_t *w4,
                     int group, void *y, int32_t *acc_out, int M, int N, int K,
                     cudaStream_t stream);
 
+/* Integer-native W8A8: the qmm_w4a8 contract with signed 8-bit weights, the
+ * other integer precision BitLLM evaluates (Experiment Setup: 8-bit weights and
+ * activations, group-wise scaling, group 32).
+ *   w8   (device) int8 [N][K] (two's complement; the 8-bit bitstream), 16-byte
+ *        aligned.  Everything else as for qmm_w4a8:
+ *   acc[m][n][g] = sum_{k in g} xq[m][k] * w8[n][k]   (exact int32)
+ *   y[m][n]      = sa[m] * sum_g ws[n][g] * acc[m][n][g]   (fp32 -> fp16 RNE)
+ * 1 <= M <= 64, G in {32, 64, 128}.  Errors as for qmm_w4a8. */
+QMM_API qmm_status qmm_w8a8(const int8_t *xq, const void *sa, const int8_t *w8, const void *ws,
+                            int group, void *y, int32_t *acc_out, int M, int N, int K,
+                            cudaStream_t stream);
+
 /* Per-token int8 quantization of fp16 activations, the step before qmm_w4a8
  * (BitLLM sec. 2.2, Eq. (1): q = clip(round(x / s) + z, q_min, q_max), with
  * the int8 range of Fig. 2(a)).  Reading of the pages (which do not fix how s

@@ -92,6 +92,15 @@ def test_gemm_and_w4a8_argument_errors(lib):
     assert lib.qmm_w4a8(_fake(0x10004), A16, B16, A16, 128, B16, None, 1, 64, 128, None) == 4
 
 
+def test_w8a8_argument_errors(lib):
+    assert lib.qmm_w8a8(A16, A16, B16, A16, 48, B16, None, 1, 64, 128, None) == 3   # group
+    assert lib.qmm_w8a8(A16, A16, B16, A16, 32, B16, None, 65, 64, 128, None) == 3  # M <= 64
+    assert lib.qmm_w8a8(A16, A16, B16, A16, 32, B16, None, 1, 64, 100, None) == 3   # K % group
+    assert lib.qmm_w8a8(A16, A16, None, A16, 32, B16, None, 1, 64, 128, None) == 1
+    assert lib.qmm_w8a8(A16, A16, _fake(0x20008), A16, 32, B16, None, 1, 64, 128, None) == 4
+    assert lib.qmm_w8a8(A16, A16, B16, A16, 32, B16, None, 0, 64, 128, None) == 0
+
+
 def test_quantize_act_argument_errors(lib):
     assert lib.qmm_quantize_act(A16, B16, A16, 2, 12, None) == 3            # K % 8
     assert lib.qmm_quantize_act(A16, B16, A16, -1, 64, None) == 3
