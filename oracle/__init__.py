@@ -16,7 +16,9 @@ arrays.  Citations for each step are in the C file's header:
 * W4A8 integer core ``r + sum a_i b_i`` per group and fp64 epilogue --
   BitLLM sec. 4.3 (dp4a), sec. 4.4 (deferred dequantization, Fig. 9); the
   same core with signed 8-bit weights is W8A8 (BitLLM, Experiment Setup);
-* per-token int8 quantization of fp16 activations -- BitLLM sec. 2.2 Eq. (1).
+* per-token int8 quantization of fp16 activations -- BitLLM sec. 2.2 Eq. (1);
+* signed b-bit weights: the sign-bit flip between two's complement and offset
+  binary, and the signed dequantize-then-matmul.
 
 Every function here is pinned by a ``-m "not gpu"`` test (hand-packed
 examples, round trips, brute force with Python integers/fractions, closed
@@ -74,6 +76,8 @@ def _load():
             lib.oracle_wxa8.restype = I
             lib.oracle_signed_value.argtypes = [I, I]
             lib.oracle_signed_value.restype = I
+            lib.oracle_flip_sign.argtypes = [P, L, L, I]
+            lib.oracle_flip_sign.restype = None
             lib.oracle_threads.argtypes = [I, L]
             lib.oracle_threads.restype = I
             lib.oracle_quantize_act.argtypes = [P, P, P, L, L]
@@ -239,3 +243,24 @@ def solve_w8a8(prob, want_acc=True, nthreads: int = 0):
     w = np.ascontiguousarray(prob.w8.view(np.uint8))
     return wxa8(prob.xq, prob.sa.astype(np.float64), w, 8, prob.ws.astype(np.float64),
                 prob.group, prob.K, want_acc, nthreads)
+
+
+def flip_sign(packed: np.ndarray, K: int, bits: int) -> np.ndarray:
+    """A copy of the packed stream with the top bit of every b-bit code flipped
+    (two's complement <-> offset binary)."""
+    out = np.array(_c(packed, np.uint8), copy=True)
+    if out.shape[1] * 8 != K * bits:
+        raise ValueError("packed row length must be K*bits/8")
+    _load().oracle_flip_sign(_ptr(out), out.shape[0], K, bits)
+    return out
+
+
+def qmm_signed(x_f64: np.ndarray, packed: np.ndarray, bits: int, group: int, scales: np.ndarray,
+               K: int) -> np.ndarray:
+    """fp64 y = x . W^T with W[n][k] = c[n][k] * s[n][k/G], c the two's-complement
+    value of code k of column n (no zero point).  numpy's matmul is the last step."""
+    codes = unpack(packed, K, bits)
+    lib = _load()
+    table = np.array([lib.oracle_signed_value(c, bits) for c in range(1 << bits)], dtype=np.float64)
+    w = table[codes] * np.repeat(_c(scales, np.float64), group, axis=1)
+    return _c(x_f64, np.float64) @ w.T

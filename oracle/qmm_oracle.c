@@ -27,6 +27,12 @@
  *     epilogue is y = sa[m] * sum_g ws[n][g] * acc[m][n][g] in fp64.  The
  *     same core with signed 8-bit weights (two's-complement bytes) is the
  *     W8A8 precision BitLLM evaluates beside W4A8 (Experiment Setup).
+ *  6. Signed b-bit weights (Tilus review: signed integer types of any width
+ *     among the arbitrary low-precision types).  A code is b-bit two's
+ *     complement, w = c * s with no zero point.  Flipping the top bit of
+ *     every code (c xor 2^(b-1), "offset binary") turns such a stream into one
+ *     whose unsigned codes u satisfy c = u - 2^(b-1): oracle_flip_sign flips
+ *     stream bit k*b + b-1 of every code k, one bit at a time.
  *  5. Per-token int8 quantization of fp16 activations (BitLLM sec. 2.2,
  *     Eq. (1), q = clip(round(x/s) + z, q_min, q_max), with the int8 range
  *     of Fig. 2(a)).  Reading: symmetric per token (z = 0), s = the token's
@@ -292,6 +298,20 @@ void oracle_quantize_act(const uint16_t *x, int8_t *xq, uint16_t *sa, long M, lo
                     q = 127.0f;
             }
             xq[m * K + k] = (int8_t)q;
+        }
+    }
+}
+
+/* ---- 6. signed weights: flip the top bit of every code ------------------ */
+
+void oracle_flip_sign(uint8_t *packed, long N, long K, int bits)
+{
+    const long row_bytes = K * bits / 8;
+    for (long n = 0; n < N; ++n) {
+        uint8_t *row = packed + n * row_bytes;
+        for (long k = 0; k < K; ++k) {
+            const long i = k * bits + bits - 1;   /* the code's top stream bit */
+            row[i >> 3] ^= (uint8_t)(1u << (i & 7));
         }
     }
 }

@@ -335,3 +335,43 @@ def test_wxa8_at_four_bits_is_w4a8():
                               prob.group, prob.K)
     np.testing.assert_array_equal(acc4, accx)
     np.testing.assert_array_equal(y4, yx)
+
+
+# ---- signed b-bit weights: sign flip and the signed matmul ---------------------------------
+@pytest.mark.parametrize("case", list(_golden_lines("sign_flip_masks.txt")))
+def test_sign_flip_masks(case):
+    bits = int(case[0])
+    mask = [int(v, 16) for v in case[1].split()]
+    K = 64
+    flipped = oracle.flip_sign(np.zeros((1, K * bits // 8), dtype=np.uint8), K, bits)[0]
+    assert flipped.tolist() == mask * (K // 8)
+
+
+@pytest.mark.parametrize("bits", range(1, 9))
+def test_sign_flip_is_an_involution_and_maps_codes(bits):
+    st = SplitMix64(bits)
+    N, K = 3, 96
+    codes = st.uniform_bits(N * K, bits).reshape(N, K)
+    packed, _ = oracle.pack(codes, bits)
+    once = oracle.flip_sign(packed, K, bits)
+    np.testing.assert_array_equal(oracle.flip_sign(once, K, bits), packed)
+    np.testing.assert_array_equal(oracle.unpack(once, K, bits), codes ^ (1 << (bits - 1)))
+
+
+@pytest.mark.parametrize("bits", [1, 3, 4, 6, 8])
+def test_signed_matmul_is_offset_binary_with_half_range_zero(bits):
+    st = SplitMix64(100 + bits)
+    M, N, K, G = 2, 5, 128, 32
+    codes = st.uniform_bits(N * K, bits).reshape(N, K)
+    packed, _ = oracle.pack(codes, bits)
+    s = (0.02 * np.abs(st.normal(N * K // G)) + 1e-3).astype(np.float16).reshape(N, K // G)
+    x = st.normal(M * K).reshape(M, K).astype(np.float16).astype(np.float64)
+    y_signed = oracle.qmm_signed(x, packed, bits, G, s.astype(np.float64), K)
+    # explicit two's-complement weights from Python integers
+    c = np.where(codes >= (1 << (bits - 1)), codes.astype(np.int64) - (1 << bits), codes)
+    w = c * np.repeat(s.astype(np.float64), G, axis=1)
+    np.testing.assert_allclose(y_signed, x @ w.T, rtol=1e-12, atol=1e-12)
+    # the same through the unsigned definition: flipped stream, zero 2^(b-1)
+    y_off = oracle.qmm(x, oracle.flip_sign(packed, K, bits), bits, G, s.astype(np.float64), None,
+                       1 << (bits - 1), K)
+    np.testing.assert_allclose(y_off, y_signed, rtol=1e-12, atol=1e-12)
