@@ -40,6 +40,7 @@ SIGNATURES = {
     "qmm_gemm": ([_P, _I, _P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P], _I),
     "qmm_w4a8": ([_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P], _I),
     "qmm_w8a8": ([_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P], _I),
+    "qmm_flip_sign": ([_P, _I, _I, _I, _P], _I),
     "qmm_quantize_act": ([_P, _P, _P, _I, _I, _P], _I),
     "qmm_device_status": ([_P], _I),
     "qmm_watchdog_selftest": ([_P], _I),
@@ -187,6 +188,18 @@ def qmm_w4a8(xq, sa, w4, ws, group=128, want_acc=False, out=None, acc_out=None):
     _check(load().qmm_w4a8(_ptr(xq), _ptr(sa), _ptr(w4), _ptr(ws), group, _ptr(out),
                            _ptr(acc_out), M, N, K, _stream(xq.device)), "qmm_w4a8")
     return (out, acc_out) if want_acc else out
+
+
+def qmm_flip_sign(packed, K, bits):
+    """Flips the top bit of every b-bit code of `packed` ([N][K*bits/8]) in place:
+    signed two's-complement codes become offset-binary codes for qmm_gemv /
+    qmm_gemm with zero_const = 2**(bits-1).  Returns `packed`."""
+    _dev(packed, "packed", torch.uint8)
+    N = packed.shape[0]
+    if packed.shape[1] * 8 != K * bits:
+        raise ValueError("packed must be [N][K*bits/8]")
+    _check(load().qmm_flip_sign(_ptr(packed), N, K, bits, _stream(packed.device)), "qmm_flip_sign")
+    return packed
 
 
 def qmm_w8a8(xq, sa, w8, ws, group=32, want_acc=False, out=None, acc_out=None):

@@ -228,6 +228,22 @@ qmm_status qmm_unpack(const uint8_t *packed, uint8_t *codes, int N, int K, int b
     return from_cuda(launch_unpack(packed, codes, N, K, bits, stream, f->num_sms));
 }
 
+qmm_status qmm_flip_sign(uint8_t *packed, int N, int K, int bits, cudaStream_t stream)
+{
+    if (bits < 1 || bits > 8)
+        return QMM_ERR_BITS;
+    if (N < 0 || K < 0 || (static_cast<long long>(K) * bits) % 8)
+        return QMM_ERR_SHAPE;
+    if (N == 0 || K == 0)
+        return QMM_OK;
+    if (!packed)
+        return QMM_ERR_NULL;
+    const DeviceFacts *f = device_facts();
+    if (!f || f->usable != QMM_OK)
+        return QMM_ERR_DEVICE;
+    return from_cuda(launch_flip_sign(packed, N, K, bits, stream, f->num_sms));
+}
+
 qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int bits,
                     int group, const void *scales, const uint8_t *zeros, int zero_const,
                     void *y, qmm_dtype y_dtype, int M, int N, int K, cudaStream_t stream)

@@ -3,7 +3,7 @@
 // Column n's stream is K*b/8 bytes; code k occupies stream bits [k*b, k*b+b)
 // and stream bit i is bit (i mod 8) of byte i/8.  Packing is not on the timed
 // decode path, so these kernels favour simplicity: one thread per output
-// byte (pack) or per code (unpack).
+// byte (pack, sign flip) or per code (unpack).
 #include "common.cuh"
 
 namespace qmm {
@@ -61,6 +61,34 @@ __global__ void unpack_kernel(const uint8_t *__restrict__ packed, uint8_t *__res
             v |= static_cast<uint32_t>(row[byte + 1]) << 8;
         codes[idx] = static_cast<uint8_t>((v >> (b0 & 7)) & mask);
     }
+}
+
+// Flips the top bit of every b-bit code in place: byte j of a row is XORed
+// with the bits p in [8j, 8j + 8) that are a code's top bit, (p + 1) % b == 0
+// (codes restart at each row, which starts byte-aligned).
+__global__ void flip_sign_kernel(uint8_t *__restrict__ packed, long long N, long long K, int bits)
+{
+    const long long row_bytes = K * bits / 8;
+    const long long total = N * row_bytes;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long bit0 = 8 * (idx % row_bytes);
+        uint32_t m = 0;
+        for (int t = 0; t < 8; ++t)
+            if ((bit0 + t + 1) % bits == 0)
+                m |= 1u << t;
+        packed[idx] ^= static_cast<uint8_t>(m);
+    }
+}
+
+cudaError_t launch_flip_sign(uint8_t *packed, int N, int K, int bits, cudaStream_t stream, int num_sms)
+{
+    const long long total = (long long)N * K * bits / 8;
+    long long blocks = (total + 255) / 256;
+    if (blocks > (long long)num_sms * 16)
+        blocks = (long long)num_sms * 16;
+    flip_sign_kernel<<<(int)blocks, 256, 0, stream>>>(packed, N, K, bits);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_pack(const uint8_t *codes, uint8_t *packed, int N, int K, int bits,

@@ -141,6 +141,18 @@ QMM_API qmm_status qmm_w4a8(const int8_t *xq, const void *sa, const uint8_t *w4,
                     int group, void *y, int32_t *acc_out, int M, int N, int K,
                     cudaStream_t stream);
 
+/* Signed b-bit weights.  Flips, in place, the top bit of every b-bit code of
+ * a packed stream [N][K*bits/8] (two's complement <-> offset binary).  A
+ * stream of signed codes c (w = c * s, the signed integer types among the
+ * Tilus review's arbitrary low-precision types) becomes one of unsigned codes
+ * u = c xor 2^(b-1) with c = u - 2^(b-1), so qmm_gemv / qmm_gemm with
+ * zero_const = 2^(b-1) compute the signed matmul exactly.  An offline step
+ * like qmm_pack; applying it twice restores the stream.
+ *   packed (device) uint8 [N][K*bits/8], modified in place.
+ * Errors: QMM_ERR_BITS, QMM_ERR_SHAPE (K*bits % 8), QMM_ERR_NULL,
+ * QMM_ERR_DEVICE, QMM_ERR_CUDA. */
+QMM_API qmm_status qmm_flip_sign(uint8_t *packed, int N, int K, int bits, cudaStream_t stream);
+
 /* Integer-native W8A8: the qmm_w4a8 contract with signed 8-bit weights, the
  * other integer precision BitLLM evaluates (Experiment Setup: 8-bit weights and
  * activations, group-wise scaling, group 32).

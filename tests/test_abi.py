@@ -92,6 +92,14 @@ def test_gemm_and_w4a8_argument_errors(lib):
     assert lib.qmm_w4a8(_fake(0x10004), A16, B16, A16, 128, B16, None, 1, 64, 128, None) == 4
 
 
+def test_flip_sign_argument_errors(lib):
+    assert lib.qmm_flip_sign(B16, 4, 8, 0, None) == 2
+    assert lib.qmm_flip_sign(B16, 4, 8, 9, None) == 2
+    assert lib.qmm_flip_sign(B16, 4, 3, 3, None) == 3     # K*bits not byte aligned
+    assert lib.qmm_flip_sign(None, 4, 8, 3, None) == 1
+    assert lib.qmm_flip_sign(None, 0, 8, 3, None) == 0
+
+
 def test_w8a8_argument_errors(lib):
     assert lib.qmm_w8a8(A16, A16, B16, A16, 48, B16, None, 1, 64, 128, None) == 3   # group
     assert lib.qmm_w8a8(A16, A16, B16, A16, 32, B16, None, 65, 64, 128, None) == 3  # M <= 64
