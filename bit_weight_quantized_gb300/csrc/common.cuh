@@ -130,16 +130,6 @@ __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 }
 
 // ---- named barriers among a subset of warps -----------------------------------
-__device__ __forceinline__ void named_sync(int id, int nthreads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-__device__ __forceinline__ void named_arrive(int id, int nthreads)
-{
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 // ---- packed fp16 arithmetic on raw 32-bit registers ----------------------------------
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t bits)
 {
@@ -160,20 +150,6 @@ __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b)
 {
     uint32_t d;
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b)
-{
-    uint32_t d;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c)
-{
-    uint32_t d;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
 
@@ -209,11 +185,6 @@ __device__ __forceinline__ float f16_bits_to_f32(uint16_t h)
     float f;
     asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
     return f;
-}
-
-__device__ __forceinline__ float bf16_bits_to_f32(uint16_t h)
-{
-    return __uint_as_float(static_cast<uint32_t>(h) << 16);
 }
 
 }  // namespace qmm

@@ -618,7 +618,7 @@ skinny_kernel(const GemvParams p)
                             const int lg = lc * NGC + gi;
                             const uint16_t *xg = xp + (lc * NGC + gi) * gstride;
                             // activation fragments of the R/4 MMAs, shared by the tiles
-                            uint32_t bf[NT <= 2 ? R / 4 : 1][NT <= 2 ? NT : 1][2];
+                            [[maybe_unused]] uint32_t bf[NT <= 2 ? R / 4 : 1][NT <= 2 ? NT : 1][2];
                             if constexpr (NT <= 2) {
 #pragma unroll
                                 for (int nt = 0; nt < NT; ++nt)
@@ -631,7 +631,8 @@ skinny_kernel(const GemvParams p)
                                         bf[j + 1][nt][1] = v.w;
                                     }
                             }
-                            float2 xv[NT], cv[NT];
+                            float2 xv[NT];
+                            [[maybe_unused]] float2 cv[NT];   // MODE 0 only
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt) {
                                 xv[nt] = *reinterpret_cast<const float2 *>(xs + lg * MP + 8 * nt + 2 * t);
@@ -673,8 +674,8 @@ skinny_kernel(const GemvParams p)
 #pragma unroll
                                     for (int e = 0; e < 4; ++e)
                                         d[i][0][e] = d[i][1][e] = 0.f;
-#pragma unroll
                                 uint4 bv = make_uint4(0u, 0u, 0u, 0u);   // NT > 2: chunk of j, j + 1
+#pragma unroll
                                 for (int j = 0; j < R / 4; ++j) {
                                     uint32_t b0, b1;
                                     if constexpr (NT <= 2) {
