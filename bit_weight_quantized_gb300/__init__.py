@@ -49,6 +49,7 @@ SIGNATURES = {
 }
 
 _lib = None
+_FN = {}   # name -> the configured ctypes function, filled by load()
 
 
 class QmmError(RuntimeError):
@@ -69,6 +70,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = res
+            _FN[name] = fn
         _lib = lib
     return _lib
 
@@ -79,31 +81,33 @@ def _check(status: int, where: str):
 
 
 def _ptr(t: Optional[torch.Tensor]):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # a plain int: ctypes converts it for a c_void_p argument without an object
+    return None if t is None else t.data_ptr()
 
 
 _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(device=None):
-    # the raw handle of the current stream, without building a Stream object;
-    # `device` is a device index, a torch.device or None (the current device)
+    # the raw handle (an int) of the current stream, without building a Stream
+    # object; `device` is a device index, a torch.device or None (the current one)
     if _raw_stream is not None:
         idx = device.index if isinstance(device, torch.device) else device
         if idx is None:
             idx = torch.cuda.current_device()
-        return ctypes.c_void_p(_raw_stream(idx))
-    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+        return _raw_stream(idx)
+    return torch.cuda.current_stream(device).cuda_stream
 
 
 def _dev(t: torch.Tensor, name: str, dtype=None, shape=None):
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
-    if dtype is not None and t.dtype != dtype:
-        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
-    if shape is not None and tuple(t.shape) != tuple(shape):
+    if not (t.is_cuda and t.is_contiguous()) or (dtype is not None and t.dtype != dtype) or (
+            shape is not None and t.shape != shape):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if dtype is not None and t.dtype != dtype:
+            raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     return t
 
@@ -151,10 +155,12 @@ def _qmm(name, x, packed, bits, group, scales, zeros, zero_const, out, out_dtype
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=x.device)
     _dev(out, "out", out_dtype, (M, N))
-    fn = getattr(load(), name)
-    _check(fn(x.data_ptr(), _DT[x.dtype], packed.data_ptr(), bits, group, scales.data_ptr(),
-              None if zeros is None else zeros.data_ptr(), int(zero_const), out.data_ptr(),
-              _DT[out_dtype], M, N, K, _stream(x.get_device())), name)
+    fn = _FN.get(name) or getattr(load(), name)
+    st = fn(x.data_ptr(), _DT[x.dtype], packed.data_ptr(), bits, group, scales.data_ptr(),
+            None if zeros is None else zeros.data_ptr(), int(zero_const), out.data_ptr(),
+            _DT[out_dtype], M, N, K, _stream(x.get_device()))
+    if st:
+        raise QmmError(st, name)
     return out
 
 
@@ -241,7 +247,7 @@ def qmm_quantize_act(x, xq=None, sa=None):
 
 def qmm_device_status(stream=None) -> int:
     """Synchronizes the stream and returns (and clears) the device status word."""
-    s = ctypes.c_void_p(stream.cuda_stream) if stream is not None else _stream()
+    s = stream.cuda_stream if stream is not None else _stream()
     return load().qmm_device_status(s)
 
 
