@@ -18,7 +18,9 @@ arrays.  Citations for each step are in the C file's header:
   same core with signed 8-bit weights is W8A8 (BitLLM, Experiment Setup);
 * per-token int8 quantization of fp16 activations -- BitLLM sec. 2.2 Eq. (1);
 * signed b-bit weights: the sign-bit flip between two's complement and offset
-  binary, and the signed dequantize-then-matmul.
+  binary, and the signed dequantize-then-matmul;
+* float b-bit weights (1 sign, e exponent, m mantissa bits) and their
+  dequantize-then-matmul.
 
 Every function here is pinned by a ``-m "not gpu"`` test (hand-packed
 examples, round trips, brute force with Python integers/fractions, closed
@@ -78,6 +80,8 @@ def _load():
             lib.oracle_signed_value.restype = I
             lib.oracle_flip_sign.argtypes = [P, L, L, I]
             lib.oracle_flip_sign.restype = None
+            lib.oracle_float_value.argtypes = [I, I, I]
+            lib.oracle_float_value.restype = ctypes.c_double
             lib.oracle_threads.argtypes = [I, L]
             lib.oracle_threads.restype = I
             lib.oracle_quantize_act.argtypes = [P, P, P, L, L]
@@ -262,5 +266,20 @@ def qmm_signed(x_f64: np.ndarray, packed: np.ndarray, bits: int, group: int, sca
     codes = unpack(packed, K, bits)
     lib = _load()
     table = np.array([lib.oracle_signed_value(c, bits) for c in range(1 << bits)], dtype=np.float64)
+    w = table[codes] * np.repeat(_c(scales, np.float64), group, axis=1)
+    return _c(x_f64, np.float64) @ w.T
+
+
+def float_value(code: int, ebits: int, mbits: int) -> float:
+    return _load().oracle_float_value(int(code), ebits, mbits)
+
+
+def qmm_float(x_f64: np.ndarray, packed: np.ndarray, ebits: int, mbits: int, group: int,
+              scales: np.ndarray, K: int) -> np.ndarray:
+    """fp64 y = x . W^T with W[n][k] = value(code[n][k]) * s[n][k/G] for float codes of
+    1 + ebits + mbits bits.  numpy's matmul is the last step."""
+    bits = 1 + ebits + mbits
+    codes = unpack(packed, K, bits)
+    table = np.array([float_value(c, ebits, mbits) for c in range(1 << bits)], dtype=np.float64)
     w = table[codes] * np.repeat(_c(scales, np.float64), group, axis=1)
     return _c(x_f64, np.float64) @ w.T

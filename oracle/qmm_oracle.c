@@ -33,6 +33,12 @@
  *     every code (c xor 2^(b-1), "offset binary") turns such a stream into one
  *     whose unsigned codes u satisfy c = u - 2^(b-1): oracle_flip_sign flips
  *     stream bit k*b + b-1 of every code k, one bit at a time.
+ *  7. Float b-bit weights (Tilus review: float3-float8 among the arbitrary
+ *     low-precision types; the pages fix no exponent / mantissa split and no
+ *     special values).  Reading: a code is 1 sign bit, e exponent bits and m
+ *     mantissa bits (b = 1 + e + m, top to bottom), bias 2^(e-1) - 1, every
+ *     encoding finite: E > 0 gives (-1)^s 2^(E - bias) (1 + M / 2^m), E = 0
+ *     gives (-1)^s 2^(1 - bias) M / 2^m.  w = value * s per group.
  *  5. Per-token int8 quantization of fp16 activations (BitLLM sec. 2.2,
  *     Eq. (1), q = clip(round(x/s) + z, q_min, q_max), with the int8 range
  *     of Fig. 2(a)).  Reading: symmetric per token (z = 0), s = the token's
@@ -314,4 +320,21 @@ void oracle_flip_sign(uint8_t *packed, long N, long K, int bits)
             row[i >> 3] ^= (uint8_t)(1u << (i & 7));
         }
     }
+}
+
+/* ---- 7. float weights ---------------------------------------------------- */
+
+double oracle_float_value(int code, int ebits, int mbits)
+{
+    const int b = 1 + ebits + mbits;
+    const int sign = (code >> (b - 1)) & 1;
+    const int E = (code >> mbits) & ((1 << ebits) - 1);
+    const int M = code & ((1 << mbits) - 1);
+    const int bias = (1 << (ebits - 1)) - 1;
+    double v;
+    if (E > 0)
+        v = ldexp(1.0 + (double)M / (double)(1 << mbits), E - bias);
+    else
+        v = ldexp((double)M / (double)(1 << mbits), 1 - bias);
+    return sign ? -v : v;
 }

@@ -375,3 +375,51 @@ def test_signed_matmul_is_offset_binary_with_half_range_zero(bits):
     y_off = oracle.qmm(x, oracle.flip_sign(packed, K, bits), bits, G, s.astype(np.float64), None,
                        1 << (bits - 1), K)
     np.testing.assert_allclose(y_off, y_signed, rtol=1e-12, atol=1e-12)
+
+
+# ---- float weight codes (Tilus review: float3-float8) --------------------------------------
+@pytest.mark.parametrize("case", list(_golden_lines("float_code_values.txt")))
+def test_float_code_worked_values(case):
+    e, m = (int(v) for v in case[0].split())
+    codes = [int(v) for v in case[1].split()]
+    values = [float(v) for v in case[2].split()]
+    assert [oracle.float_value(c, e, m) for c in codes] == values
+
+
+def _float_fraction(code, e, m):
+    """The definition with exact rationals (an independent implementation)."""
+    b = 1 + e + m
+    sign = -1 if (code >> (b - 1)) & 1 else 1
+    E = (code >> m) & ((1 << e) - 1)
+    M = code & ((1 << m) - 1)
+    bias = (1 << (e - 1)) - 1
+    if E > 0:
+        v = Fraction(2) ** (E - bias) * (1 + Fraction(M, 1 << m))
+    else:
+        v = Fraction(2) ** (1 - bias) * Fraction(M, 1 << m)
+    return sign * v
+
+
+@pytest.mark.parametrize("bits", range(2, 9))
+def test_float_values_all_splits_exact(bits):
+    for e in range(1, bits):
+        m = bits - 1 - e
+        for c in range(1 << bits):
+            assert Fraction(oracle.float_value(c, e, m)) == _float_fraction(c, e, m), (e, m, c)
+
+
+@pytest.mark.parametrize("e,m", [(2, 1), (3, 2), (2, 3), (4, 3)])
+def test_float_matmul_brute_force(e, m):
+    bits = 1 + e + m
+    st = SplitMix64(50 + bits + e)
+    M, N, K, G = 2, 3, 64, 32
+    codes = st.uniform_bits(N * K, bits).reshape(N, K)
+    packed, _ = oracle.pack(codes, bits)
+    s = (0.02 * np.abs(st.normal(N * K // G)) + 1e-3).astype(np.float16).reshape(N, K // G)
+    x = st.normal(M * K).reshape(M, K).astype(np.float16)
+    y = oracle.qmm_float(x.astype(np.float64), packed, e, m, G, s.astype(np.float64), K)
+    for mm in range(M):
+        for n in range(N):
+            exact = sum(Fraction(float(x[mm, k])) * _float_fraction(int(codes[n, k]), e, m)
+                        * Fraction(float(s[n, k // G])) for k in range(K))
+            assert abs(y[mm, n] - float(exact)) <= 1e-12 * max(1.0, abs(float(exact)))
