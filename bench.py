@@ -291,8 +291,8 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf):
     work): skinny decode (M = 16, N = 14336, b = 6, group 64), the tiled path
     (M = 128 / 512 / 2048, K = 8192, N = 28672, int4, bf16), W4A8
     (M = 1 / 16 / 64, K = N = 4096; also fed from fp16 activations through the
-    per-token int8 quantizer), W8A8 (the same shapes, group 32) and the
-    quantizer alone (K = 4096)."""
+    per-token int8 quantizer), W8A8 (the same shapes, group 32), float6 e3m2
+    weights (M = 1, K = N = 4096) and the quantizer alone (K = 4096)."""
     out = {}
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
@@ -361,6 +361,15 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf):
                                  "frac_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4),
                                  "TOPs": round(2.0 * M * N * K / ms / 1e9, 1)}
     del wsets
+    # float weights: float6 e3m2 (FP6-like), M = 1, K = N = 4096, group 128
+    fsets = [(q.qmm_pack(codes(N, K, 6), 6), scales(N, K // 128)) for _ in range(8)]
+    x = torch.randn(1, K, device=dev, generator=gen).half()
+    y = torch.empty(1, N, dtype=torch.float16, device=dev)
+    ms = time_graph(torch, stream, [lambda w=w_: q.qmm_gemv_float(x, w[0], 3, 2, 128, w[1], out=y) for w_ in fsets])
+    nbytes = N * K * 6 // 8 + N * (K // 128) * 2 + K * 2 + N * 2
+    out["float6_e3m2_M1"] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
+                             "frac_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4)}
+    del fsets
     # per-token int8 activation quantizer alone: K = 4096, inputs rotate over 8 copies
     K = 4096
     for M in (1, 64, 2048):

@@ -41,6 +41,7 @@ SIGNATURES = {
     "qmm_w4a8": ([_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P], _I),
     "qmm_w8a8": ([_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P], _I),
     "qmm_flip_sign": ([_P, _I, _I, _I, _P], _I),
+    "qmm_gemv_float": ([_P, _P, _I, _I, _I, _P, _P, _I, _I, _I, _P], _I),
     "qmm_quantize_act": ([_P, _P, _P, _I, _I, _P], _I),
     "qmm_device_status": ([_P], _I),
     "qmm_watchdog_selftest": ([_P], _I),
@@ -194,6 +195,25 @@ def qmm_w4a8(xq, sa, w4, ws, group=128, want_acc=False, out=None, acc_out=None):
     _check(load().qmm_w4a8(_ptr(xq), _ptr(sa), _ptr(w4), _ptr(ws), group, _ptr(out),
                            _ptr(acc_out), M, N, K, _stream(xq.device)), "qmm_w4a8")
     return (out, acc_out) if want_acc else out
+
+
+def qmm_gemv_float(x, packed, ebits, mbits, group, scales, out=None):
+    """y[M][N] = x . W^T (fp16, 1 <= M <= 16) for float weight codes of
+    1 + ebits + mbits bits (sign, exponent, mantissa; all encodings finite)."""
+    _dev(x, "x", torch.float16)
+    M, K = x.shape
+    bits = 1 + ebits + mbits
+    _dev(packed, "packed", torch.uint8)
+    N = packed.shape[0]
+    if packed.shape[1] * 8 != K * bits:
+        raise ValueError("packed must be [N][K*bits/8]")
+    _dev(scales, "scales", torch.float16, (N, K // group))
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _dev(out, "out", torch.float16, (M, N))
+    _check(load().qmm_gemv_float(_ptr(x), _ptr(packed), ebits, mbits, group, _ptr(scales), _ptr(out),
+                                 M, N, K, _stream(x.device)), "qmm_gemv_float")
+    return out
 
 
 def qmm_flip_sign(packed, K, bits):

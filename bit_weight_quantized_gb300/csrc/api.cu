@@ -228,6 +228,35 @@ qmm_status qmm_unpack(const uint8_t *packed, uint8_t *codes, int N, int K, int b
     return from_cuda(launch_unpack(packed, codes, N, K, bits, stream, f->num_sms));
 }
 
+qmm_status qmm_gemv_float(const void *x, const uint8_t *packed, int ebits, int mbits, int group,
+                          const void *scales, void *y, int M, int N, int K, cudaStream_t stream)
+{
+    if (ebits < 1 || mbits < 0 || 1 + ebits + mbits < 2 || 1 + ebits + mbits > 8)
+        return QMM_ERR_BITS;
+    if (M < 0 || N < 0 || K < 0 || M > 16)
+        return QMM_ERR_SHAPE;
+    if (group != 32 && group != 64 && group != 128)
+        return QMM_ERR_SHAPE;
+    if (K % group)
+        return QMM_ERR_SHAPE;
+    if (M == 0 || N == 0)
+        return QMM_OK;
+    if (!y)
+        return QMM_ERR_NULL;
+    if (K > 0 && (!x || !packed || !scales))
+        return QMM_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(packed, 4) || !aligned(scales, 2) || !aligned(y, 2))
+        return QMM_ERR_ALIGN;
+    const DeviceFacts *f = device_facts();
+    if (!f || f->usable != QMM_OK)
+        return QMM_ERR_DEVICE;
+    if (K == 0)
+        return from_cuda(cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * 2, stream));
+    return from_cuda(launch_gemv_fp(static_cast<const uint16_t *>(x), packed, ebits, mbits, group,
+                                    static_cast<const uint16_t *>(scales), static_cast<uint16_t *>(y), M, N,
+                                    K, stream));
+}
+
 qmm_status qmm_flip_sign(uint8_t *packed, int N, int K, int bits, cudaStream_t stream)
 {
     if (bits < 1 || bits > 8)

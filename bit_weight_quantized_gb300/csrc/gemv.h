@@ -59,6 +59,9 @@ cudaError_t gemv_launch_w8(const GemvParams &, int, int, cudaStream_t);
 cudaError_t w4a8_launch(const GemvParams &, int, int, cudaStream_t);
 cudaError_t w8a8_launch(const GemvParams &, int, int, cudaStream_t);
 
+// fpgemv.cu: decode matmul with float weight codes (1 sign, e exponent, m mantissa bits).
+cudaError_t launch_gemv_fp(const uint16_t *x, const uint8_t *packed, int ebits, int mbits, int group,
+                           const uint16_t *scales, uint16_t *y, int M, int N, int K, cudaStream_t stream);
 // quant.cu: per-token int8 quantization of fp16 activations (one CTA per token).
 cudaError_t launch_quantize_act(const uint16_t *x, int8_t *xq, uint16_t *sa, int M, int K,
                                 cudaStream_t stream);

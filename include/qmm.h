@@ -141,6 +141,24 @@ QMM_API qmm_status qmm_w4a8(const int8_t *xq, const void *sa, const uint8_t *w4,
                     int group, void *y, int32_t *acc_out, int M, int N, int K,
                     cudaStream_t stream);
 
+/* Float weight codes (the float3-float8 types of the Tilus review's arbitrary
+ * low-precision types; the pages fix no exponent / mantissa split and no
+ * special values).  Reading: a code of b = 1 + ebits + mbits bits holds a sign
+ * bit, ebits exponent bits and mbits mantissa bits (top to bottom), bias
+ * 2^(ebits-1) - 1, and every encoding is finite:
+ *   E > 0: (-1)^s 2^(E - bias) (1 + M / 2^mbits),  E = 0: (-1)^s 2^(1 - bias) M / 2^mbits,
+ * W[n][k] = value(code k of column n) * scales[n][k/G], y = x . W^T.
+ *   x       (device) fp16 [M][K], 16-byte aligned; 1 <= M <= 16.
+ *   packed  (device) uint8 [N][K*b/8]: the b-bit stream of qmm_pack, 4-byte aligned.
+ *   scales  (device) fp16 [N][K/G]; G in {32, 64, 128}, K % G == 0.
+ *   y       (device) fp16 [M][N], fully overwritten (fp32 accumulation, RNE).
+ * Products of a weight and an activation are exact in fp32; the sums round.
+ * Errors: QMM_ERR_BITS (ebits < 1 or b outside 2..8), QMM_ERR_SHAPE,
+ * QMM_ERR_NULL, QMM_ERR_ALIGN, QMM_ERR_DEVICE, QMM_ERR_CUDA. */
+QMM_API qmm_status qmm_gemv_float(const void *x, const uint8_t *packed, int ebits, int mbits,
+                                  int group, const void *scales, void *y, int M, int N, int K,
+                                  cudaStream_t stream);
+
 /* Signed b-bit weights.  Flips, in place, the top bit of every b-bit code of
  * a packed stream [N][K*bits/8] (two's complement <-> offset binary).  A
  * stream of signed codes c (w = c * s, the signed integer types among the

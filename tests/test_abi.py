@@ -92,6 +92,16 @@ def test_gemm_and_w4a8_argument_errors(lib):
     assert lib.qmm_w4a8(_fake(0x10004), A16, B16, A16, 128, B16, None, 1, 64, 128, None) == 4
 
 
+def test_gemv_float_argument_errors(lib):
+    assert lib.qmm_gemv_float(A16, B16, 0, 3, 32, A16, B16, 1, 64, 128, None) == 2    # ebits >= 1
+    assert lib.qmm_gemv_float(A16, B16, 5, 3, 32, A16, B16, 1, 64, 128, None) == 2    # 9 bits
+    assert lib.qmm_gemv_float(A16, B16, 3, 2, 32, A16, B16, 17, 64, 128, None) == 3   # M <= 16
+    assert lib.qmm_gemv_float(A16, B16, 3, 2, 48, A16, B16, 1, 64, 128, None) == 3    # group
+    assert lib.qmm_gemv_float(None, B16, 3, 2, 32, A16, B16, 1, 64, 128, None) == 1
+    assert lib.qmm_gemv_float(_fake(0x10008), B16, 3, 2, 32, A16, B16, 1, 64, 128, None) == 4
+    assert lib.qmm_gemv_float(A16, B16, 3, 2, 32, A16, B16, 0, 64, 128, None) == 0
+
+
 def test_flip_sign_argument_errors(lib):
     assert lib.qmm_flip_sign(B16, 4, 8, 0, None) == 2
     assert lib.qmm_flip_sign(B16, 4, 8, 9, None) == 2
