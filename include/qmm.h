@@ -1,6 +1,8 @@
 /*
  * qmm.h -- C ABI of libqmm: FP16/BF16 activations x b-bit quantized weights
- * (b = 1..8), and the integer-native W4A8 variant, on one GB300 (sm_103a).
+ * (b = 1..8), the integer-native W4A8 / W8A8 variants with their per-token
+ * activation quantizer, and signed and float weight codes, on one GB300
+ * (sm_103a).
  *
  * The operation (Tilus review, lead and pith_extraction.core_discovery: a
  * matmul of FP16 activations by weights of any width from 1 to 8 bits that

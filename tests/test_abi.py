@@ -26,7 +26,8 @@ def declared_symbols():
 
 def test_header_declares_the_calls():
     syms = declared_symbols()
-    for name in ("qmm_pack", "qmm_unpack", "qmm_gemv", "qmm_gemm", "qmm_w4a8",
+    for name in ("qmm_pack", "qmm_unpack", "qmm_gemv", "qmm_gemm", "qmm_w4a8", "qmm_w8a8",
+                 "qmm_quantize_act", "qmm_flip_sign", "qmm_gemv_float",
                  "qmm_device_status", "qmm_status_string", "qmm_abi_version"):
         assert name in syms
 
