@@ -14,8 +14,10 @@
 // One warp per output column; lane l takes the 32-code runs l, l + 32, ... of
 // the column's stream (a run is b whole 32-bit words, so the warp's loads are
 // contiguous), multiplies the run by the tokens' activations, applies the
-// run's group scale and finally the warp reduces in a fixed order.  Compute-
-// light per byte: FFMA per code and token, no tensor cores (M <= 16 rows of x).
+// run's group scale and finally the warp reduces in a fixed order.  Before
+// waiting for the preceding kernel each lane prefetches its runs into L2 (the
+// weights are not that kernel's output).  Compute-light per byte: FFMA per
+// code and token, no tensor cores (M <= 16 rows of x).
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -36,16 +38,20 @@ gemv_fp_kernel(const uint16_t *__restrict__ x, const uint32_t *__restrict__ pack
 {
     if (threadIdx.x == 0)
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // x may be the output of the preceding kernel on the stream
-    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     const int n = blockIdx.x * (kFpThreads / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (n >= N)
-        return;
     const int nruns = K / 32;
     const int ng = K >> group_log2;
-    const uint32_t *row = packed + static_cast<long long>(n) * nruns * B;
+    const uint32_t *row = packed + static_cast<long long>(min(n, N - 1)) * nruns * B;
+    // the weights are not written by the preceding kernel: pull this lane's runs
+    // into L2 while it may still be running
+    for (int run = lane; run < nruns; run += 32)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(row + run * B));
+    // x may be the output of the preceding kernel on the stream
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (n >= N)
+        return;
     const uint32_t mag_mask = (1u << (B - 1)) - 1u;
     const int mshift = 23 - mbits;
 
