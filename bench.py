@@ -46,7 +46,7 @@ WORKLOAD = ("decode GEMV width sweep: M=1, K=N=4096, bits 1..8, group 128, "
             "z=2^(b-1), fp16 activations/outputs, fp32 accumulation")
 BITS = list(range(1, 9))
 PROFILE = os.path.join(ROOT, "profiles", "qmm_gemv_decode_sweep.txt")
-KERNEL_SOURCES = ["skinny.cuh", "gemv.cu", "gemv.h", "common.cuh", "unpack_plans.h"]
+KERNEL_SOURCES = ["decode.cu", "decode.h", "common.cuh"]
 
 
 def kernel_source_digest() -> str:
@@ -285,10 +285,11 @@ def time_graph(torch, stream, launches, reps: int = 10):
     return a.elapsed_time(b) / (reps * len(launches))
 
 
-def measure_others(torch, q, dev, stream, peak_gbs, peak_tf):
+def measure_others(torch, q, dev, stream, peak_gbs, peak_tf, gemv_kernel="auto"):
     """The other workload families, timed the same way on device-generated
     inputs of the workloads' shapes and laws (the values do not change the
-    work): skinny decode (M = 16, N = 14336, b = 6, group 64), the tiled path
+    work): skinny decode (M = 16, N = 14336, b = 6, group 64), the decode
+    kernel beside the skinny kernel (M = 1 and 8, K = N = 4096, b = 4), the tiled path
     (M = 128 / 512 / 2048, K = 8192, N = 28672, int4, bf16), W4A8
     (M = 1 / 16 / 64, K = N = 4096; also fed from fp16 activations through the
     per-token int8 quantizer), W8A8 (the same shapes, group 32), float6 e3m2
@@ -312,6 +313,25 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf):
     nbytes = N * K * b // 8 + N * (K // G) * 3 + M * K * 2 + M * N * 2
     out["skinny_M16_N14336_b6_g64"] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
                                        "frac_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4)}
+    del sets
+    # the decode kernel beside the skinny kernel (forced) on the decode shape
+    # K = N = 4096, b = 4, group 128, M = 1 and 8
+    N, K, b, G = 4096, 4096, 4, 128
+    sets = [(q.qmm_pack(codes(N, K, b), b), scales(N, K // G)) for _ in range(24)]
+    for M in (1, 8):
+        x = torch.randn(M, K, device=dev, generator=gen).half()
+        y = torch.empty(M, N, dtype=torch.float16, device=dev)
+        nbytes = N * K * b // 8 + N * (K // G) * 2 + M * K * 2 + M * N * 2
+        for kern in ("auto", "skinny"):
+            q.qmm_set_gemv_kernel(kern)
+            try:
+                ms = time_graph(torch, stream, [lambda s=s_: q.qmm_gemv(x, s[0], b, G, s[1], None, 8, out=y)
+                                                for s_ in sets])
+            finally:
+                q.qmm_set_gemv_kernel(gemv_kernel)
+            name = "decode" if kern == "auto" else "skinny_forced"
+            out[f"{name}_M{M}_N4096_b4_g128"] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
+                                                 "frac_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4)}
     del sets
     # tiled: K=8192, N=28672, int4 group 128, z=8, bf16
     N, K = 28672, 8192
@@ -395,6 +415,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     q.load()
+    q.qmm_set_gemv_kernel(args.gemv_kernel)
     stream = torch.cuda.Stream(device=dev)
     probs = [synthetic.decode_sweep(b) for b in BITS]
     step_bytes = sum(p.algorithmic_bytes() for p in probs)
@@ -554,7 +575,7 @@ def run_ours(args, world, rank, local):
     achieved = step_bytes / (kdur.sum() * 1e-3) / 1e9
     for k in per_width:
         per_width[k]["frac"] = round(per_width[k]["GBps"] / peak, 4)
-    traffic = profile_traffic()
+    traffic = profile_traffic() if args.gemv_kernel == "auto" else None
 
     # e2e through the public API with host buffers: every step copies the step's
     # activations (all widths, one pinned buffer) to the device, runs the eight
@@ -603,7 +624,7 @@ def run_ours(args, world, rank, local):
                 peak_tf = float(json.load(f)["bf16_tflops"])
         except Exception:
             peak_tf = 1900.0
-        others = measure_others(torch, q, dev, stream, peak, peak_tf)
+        others = measure_others(torch, q, dev, stream, peak, peak_tf, args.gemv_kernel)
         assert q.qmm_device_status(stream) == 0
 
     cpu = None
@@ -622,11 +643,14 @@ def run_ours(args, world, rank, local):
                        "step": "8 qmm_gemv calls (b=1..8), replayed from a CUDA graph",
                        "l2": f"inputs larger than L2: {copies} rotating copies of the step's "
                              f"weights ({copies * per_copy / 1e6:.0f} MB > 2 x {l2 / 1e6:.0f} MB L2)",
-                       "step_bytes": step_bytes, "parallelism": f"{world} independent replicas"},
+                       "step_bytes": step_bytes, "parallelism": f"{world} independent replicas",
+                       "gemv_kernel": args.gemv_kernel},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_kind": peak_kind,
-                         "traffic": traffic, "kernel": "qmm::skinny_kernel<b,1,32,0> (b = 1..8)",
+                         "traffic": traffic,
+                         "kernel": ("qmm::decode_kernel<b> (b = 1..8)" if args.gemv_kernel == "auto"
+                                    else "qmm::skinny_kernel<b,1,32,0> (b = 1..8)"),
                          "algorithmic_bytes_per_launch": round(step_bytes / len(probs)),
                          "frac_of_8TBs": round(achieved / 8000.0, 4),
                          "duration_source": how,
@@ -659,6 +683,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-others", action="store_true",
                     help="skip the timing of the other workload families")
+    ap.add_argument("--gemv-kernel", choices=["auto", "skinny"], default="auto",
+                    help="qmm_gemv's kernel: the default choice, or the skinny kernel forced "
+                         "for every shape (for profiling that kernel on the sweep)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

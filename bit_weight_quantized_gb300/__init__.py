@@ -43,6 +43,7 @@ SIGNATURES = {
     "qmm_flip_sign": ([_P, _I, _I, _I, _P], _I),
     "qmm_gemv_float": ([_P, _P, _I, _I, _I, _P, _P, _I, _I, _I, _P], _I),
     "qmm_quantize_act": ([_P, _P, _P, _I, _I, _P], _I),
+    "qmm_set_gemv_kernel": ([_I], _I),
     "qmm_device_status": ([_P], _I),
     "qmm_watchdog_selftest": ([_P], _I),
     "qmm_status_string": ([_I], ctypes.c_char_p),
@@ -167,8 +168,20 @@ def _qmm(name, x, packed, bits, group, scales, zeros, zero_const, out, out_dtype
 
 def qmm_gemv(x, packed, bits, group, scales, zeros=None, zero_const=0, out=None,
              out_dtype=None) -> torch.Tensor:
-    """y[M][N] = x . W^T for 1 <= M <= 16 (decode / skinny)."""
+    """y[M][N] = x . W^T for 1 <= M <= 16 (the decode or the skinny kernel)."""
     return _qmm("qmm_gemv", x, packed, bits, group, scales, zeros, zero_const, out, out_dtype)
+
+
+GEMV_KERNELS = {"auto": 0, "skinny": 1}
+
+
+def qmm_set_gemv_kernel(kernel: str):
+    """Kernel choice of qmm_gemv for the calls that follow, process-wide:
+    "auto" (the decode kernel where it applies, else the skinny kernel) or
+    "skinny" (the skinny kernel for every shape)."""
+    if kernel not in GEMV_KERNELS:
+        raise ValueError(f"kernel must be one of {sorted(GEMV_KERNELS)}")
+    _check(load().qmm_set_gemv_kernel(GEMV_KERNELS[kernel]), "qmm_set_gemv_kernel")
 
 
 def qmm_gemm(x, packed, bits, group, scales, zeros=None, zero_const=0, out=None,

@@ -3,10 +3,12 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
 #include "common.cuh"
+#include "decode.h"
 #include "gemv.h"
 #include "w4a8.h"
 #include "gemm.h"
@@ -44,6 +46,7 @@ struct DeviceFacts {
 
 DeviceFacts g_facts[kMaxDevices];
 std::mutex g_mutex;
+std::atomic<int> g_gemv_kernel{QMM_GEMV_AUTO};
 
 // Facts about the current device, computed once per device.
 const DeviceFacts *device_facts()
@@ -291,6 +294,23 @@ qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int
         return QMM_ERR_DEVICE;
     if (K == 0)
         return from_cuda(cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * 2, stream));
+    if (g_gemv_kernel.load(std::memory_order_relaxed) == QMM_GEMV_AUTO &&
+        decode_supports(M, N, K, group, f->num_sms)) {
+        DecodeParams d;
+        std::memset(&d, 0, sizeof(d));
+        d.x = static_cast<const uint16_t *>(x);
+        d.packed = packed;
+        d.scales = static_cast<const uint16_t *>(scales);
+        d.zeros = zeros;
+        d.y = y;
+        d.M = M;
+        d.N = N;
+        d.K = K;
+        d.group_log2 = group == 64 ? 6 : 7;
+        d.zero_const = zeros ? 0 : zero_const;
+        d.y_bf16 = y_dtype == QMM_BF16;
+        return from_cuda(launch_decode(d, bits, f->num_sms, stream));
+    }
 
     GemvParams p;
     std::memset(&p, 0, sizeof(p));
@@ -325,6 +345,14 @@ qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int
     default: e = gemv_launch_w8(p, grid, smem, stream); break;
     }
     return from_cuda(e);
+}
+
+qmm_status qmm_set_gemv_kernel(int kernel)
+{
+    if (kernel != QMM_GEMV_AUTO && kernel != QMM_GEMV_SKINNY)
+        return QMM_ERR_SHAPE;
+    g_gemv_kernel.store(kernel, std::memory_order_relaxed);
+    return QMM_OK;
 }
 
 qmm_status qmm_gemm(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int bits,

@@ -110,12 +110,27 @@ QMM_API qmm_status qmm_unpack(const uint8_t *packed, uint8_t *codes, int N, int 
  * activations, and accumulate each group in fp32; the group's scale and zero
  * are applied in fp32 afterwards as s*(sum q*x - z*sum x), which equals
  * sum s*(q - z)*x.  Results are deterministic run to run.
- * Activations of M x K fp16 must fit in shared memory next to the weight
- * pipeline (M*K <= 64K elements for M <= 8 and K = 4096 class shapes; larger
- * return QMM_ERR_UNSUPPORTED).  K % 32 == 0 is implied by the group rule. */
+ * Two kernels serve the call.  The decode kernel takes M <= 8, G in {64, 128},
+ * K % (8*G) == 0 and N <= 32 x the SM count: each warp reads its share of K
+ * straight from global memory into the MMA operands, with no shared-memory
+ * staging.  The skinny kernel takes every other shape: it stages the
+ * activations in shared memory, and M x K fp16 must fit there next to the
+ * weight pipeline (M*K <= 64K elements for M <= 8 and K = 4096 class shapes;
+ * larger return QMM_ERR_UNSUPPORTED).  The two sum in different orders, so
+ * their outputs may differ in the last bits.  qmm_set_gemv_kernel() forces the
+ * skinny kernel.  K % 32 == 0 is implied by the group rule. */
 QMM_API qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int bits,
                     int group, const void *scales, const uint8_t *zeros, int zero_const,
                     void *y, qmm_dtype y_dtype, int M, int N, int K, cudaStream_t stream);
+
+/* Kernel choice of qmm_gemv for the calls that follow, process-wide:
+ *   QMM_GEMV_AUTO   (0, the default) the decode kernel where it applies,
+ *                   else the skinny kernel;
+ *   QMM_GEMV_SKINNY (1) the skinny kernel for every shape.
+ * Returns QMM_ERR_SHAPE for any other value.  The setting is read when a call
+ * is issued; it does not change calls already issued. */
+typedef enum { QMM_GEMV_AUTO = 0, QMM_GEMV_SKINNY = 1 } qmm_gemv_kernel;
+QMM_API qmm_status qmm_set_gemv_kernel(int kernel);
 
 /* Tiled matmul for M >= 17 (the dense-contraction regime, Tilus review
  * supporting_citations [41]: tensor-core instruction layouts).  Same

@@ -27,7 +27,7 @@ def declared_symbols():
 def test_header_declares_the_calls():
     syms = declared_symbols()
     for name in ("qmm_pack", "qmm_unpack", "qmm_gemv", "qmm_gemm", "qmm_w4a8", "qmm_w8a8",
-                 "qmm_quantize_act", "qmm_flip_sign", "qmm_gemv_float",
+                 "qmm_quantize_act", "qmm_flip_sign", "qmm_gemv_float", "qmm_set_gemv_kernel",
                  "qmm_device_status", "qmm_status_string", "qmm_abi_version"):
         assert name in syms
 
@@ -135,6 +135,18 @@ def test_pack_argument_errors(lib):
     assert lib.qmm_pack(A16, B16, 4, 8, 0, None, None) == 2
     assert lib.qmm_pack(None, B16, 4, 8, 3, None, None) == 1
     assert lib.qmm_unpack(A16, B16, 4, 8, 9, None) == 2
+
+
+def test_gemv_kernel_choice(lib):
+    import bit_weight_quantized_gb300 as q
+    assert lib.qmm_set_gemv_kernel(2) == 3
+    assert lib.qmm_set_gemv_kernel(-1) == 3
+    assert lib.qmm_set_gemv_kernel(1) == 0
+    assert lib.qmm_set_gemv_kernel(0) == 0
+    with pytest.raises(ValueError):
+        q.qmm_set_gemv_kernel("fastest")
+    q.qmm_set_gemv_kernel("skinny")
+    q.qmm_set_gemv_kernel("auto")
 
 
 @pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="needs a machine without a GPU")
