@@ -84,8 +84,8 @@ decode_kernel(const DecodeParams p)
     const int kw = K / 8;                  // codes of this warp
     const int k0w = warp * kw;
     const int nblk = kw / 64;
-    const int blk_per_group = (1 << p.group_log2) / 64;
-    const int o = 16 * ((B * t) & 1);      // bit offset of the thread's first code in its first word
+    const int group_end = (1 << (p.group_log2 - 6)) - 1;   // blocks per group - 1 (a power of two)
+    const int o = (B & 1) ? 16 * (t & 1) : 0;   // bit offset of the thread's first code in its first word
     // this thread's rows (tile i, half h: row 16 i + 8 h + g; padding rows read row nrows - 1)
     const uint32_t *rowp[2][2];
     int rowi[2][2];
@@ -136,10 +136,11 @@ decode_kernel(const DecodeParams p)
         for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                // shift the window so that the thread's code 0 sits at bit 0
+                // shift the window so that the thread's code 0 sits at bit 0 (even widths: it does)
 #pragma unroll
                 for (int k = 0; k < NW; ++k)
-                    win[i][h][k] = __funnelshift_r(nw[i][h][k], k + 1 < NW ? nw[i][h][k + 1] : 0u, o);
+                    win[i][h][k] = (B & 1) ? __funnelshift_r(nw[i][h][k], k + 1 < NW ? nw[i][h][k + 1] : 0u, o)
+                                           : nw[i][h][k];
                 win[i][h][NW] = 0u;
             }
         const uint4 xa = nxa, xb = nxb;
@@ -166,7 +167,7 @@ decode_kernel(const DecodeParams p)
                               dec_pair<B>(win[i][0], 4 * s + 2), dec_pair<B>(win[i][1], 4 * s + 2),
                               xw[2 * s], xw[2 * s + 1]);
         }
-        if ((j + 1) % blk_per_group == 0) {   // the end of a group
+        if (((j + 1) & group_end) == 0) {   // the end of a group
             float X = xsum;                   // this quad's token, all 16 t-parts
             X += __shfl_xor_sync(0xffffffffu, X, 1);
             X += __shfl_xor_sync(0xffffffffu, X, 2);
