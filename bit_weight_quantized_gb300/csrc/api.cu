@@ -294,7 +294,7 @@ qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int
         return QMM_ERR_DEVICE;
     if (K == 0)
         return from_cuda(cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * 2, stream));
-    if (g_gemv_kernel.load(std::memory_order_relaxed) == QMM_GEMV_AUTO &&
+    if (g_gemv_kernel.load(std::memory_order_relaxed) == QMM_GEMV_AUTO && aligned(packed, 16) &&
         decode_supports(M, N, K, group, f->num_sms)) {
         DecodeParams d;
         std::memset(&d, 0, sizeof(d));

@@ -14,7 +14,8 @@
 // Work split.  CTA c owns at most 32 consecutive columns (two 16-row MMA
 // tiles); warp w owns K/8 codes of all of them, in blocks of 64.  In a block,
 // quad thread t owns codes [16t, 16t + 16) of each of its rows (b/2 words,
-// rounded up, read straight from global memory), and the MMA's k order is
+// rounded up, read straight from global memory: one 8-byte load at b = 4, one
+// 16-byte load at b = 8), and the MMA's k order is
 // permuted to match: the 16 codes of MMA step s of thread t are its codes
 // 4s .. 4s + 3, so the B fragment is x[16t + 4s .. 16t + 4s + 3] of the block,
 // one 32-byte load per thread and block.  No activation staging, no shared
@@ -61,6 +62,29 @@ __device__ __forceinline__ uint32_t dec_pair(const uint32_t (&win)[dec_words<B>(
         constexpr uint32_t magic = static_cast<uint32_t>(B + 15) << 10;   // fp16 bits of 2^B
         const uint32_t lo = lop3_and_or(u, mask, magic | (magic << 16));
         return lop3_and_or(u << (16 - B), mask << 16, lo);
+    }
+}
+
+// The thread's words of one row and block.  At b = 4 they are two words at an
+// even word index, at b = 8 four at a multiple of four (K is a multiple of 512
+// and the packed base 16-byte aligned), so one vector load reads them.
+template <int B>
+__device__ __forceinline__ void load_words(uint32_t (&w)[dec_words<B>()], const uint32_t *src)
+{
+    if constexpr (B == 8) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(src);
+        w[0] = v.x;
+        w[1] = v.y;
+        w[2] = v.z;
+        w[3] = v.w;
+    } else if constexpr (B == 4) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(src);
+        w[0] = v.x;
+        w[1] = v.y;
+    } else {
+#pragma unroll
+        for (int k = 0; k < dec_words<B>(); ++k)
+            w[k] = src[k];
     }
 }
 
@@ -125,9 +149,7 @@ decode_kernel(const DecodeParams p)
     for (int i = 0; i < 2; ++i)
 #pragma unroll
         for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int k = 0; k < NW; ++k)
-                nw[i][h][k] = rowp[i][h][k];
+            load_words<B>(nw[i][h], rowp[i][h]);
 
 #pragma unroll 1
     for (int j = 0; j < nblk; ++j) {
@@ -151,9 +173,7 @@ decode_kernel(const DecodeParams p)
             for (int i = 0; i < 2; ++i)
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int k = 0; k < NW; ++k)
-                        nw[i][h][k] = rowp[i][h][(j + 1) * 2 * B + k];
+                    load_words<B>(nw[i][h], rowp[i][h] + (j + 1) * 2 * B);
         }
         const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
 #pragma unroll

@@ -9,7 +9,7 @@ namespace qmm {
 
 struct DecodeParams {
     const uint16_t *x;        // fp16 [M][K], 16-byte aligned
-    const uint8_t *packed;    // [N][K*b/8], 4-byte aligned
+    const uint8_t *packed;    // [N][K*b/8], 16-byte aligned
     const uint16_t *scales;   // fp16 [N][K/G]
     const uint8_t *zeros;     // uint8 [N][K/G] or nullptr (then zero_const)
     void *y;                  // fp16 or bf16 [M][N]

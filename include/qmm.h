@@ -111,7 +111,8 @@ QMM_API qmm_status qmm_unpack(const uint8_t *packed, uint8_t *codes, int N, int 
  * are applied in fp32 afterwards as s*(sum q*x - z*sum x), which equals
  * sum s*(q - z)*x.  Results are deterministic run to run.
  * Two kernels serve the call.  The decode kernel takes M <= 8, G in {64, 128},
- * K % (8*G) == 0 and N <= 32 x the SM count: each warp reads its share of K
+ * K % (8*G) == 0, N <= 32 x the SM count and a 16-byte aligned `packed`: each
+ * warp reads its share of K
  * straight from global memory into the MMA operands, with no shared-memory
  * staging.  The skinny kernel takes every other shape: it stages the
  * activations in shared memory, and M x K fp16 must fit there next to the

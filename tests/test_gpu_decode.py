@@ -110,3 +110,16 @@ def test_decode_back_to_back_calls(q):
     torch.cuda.synchronize()
     p2.x = y1.cpu().numpy().astype(np.float16).reshape(1, 1024)
     assert rel_err(y_to_f64(y2), oracle_y(p2)) <= REL_TOL
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_decode_shape_with_unaligned_packed_base(q, bits):
+    # a packed base that is 4- but not 16-byte aligned goes to the skinny kernel
+    prob = synthetic.make_qmm(2, 300, 1024, bits, 128, zero_mode="half", seed=bits)
+    x, packed, scales, _ = to_dev_problem(prob)
+    buf = torch.zeros(packed.numel() + 16, dtype=torch.uint8, device="cuda")
+    shifted = buf[4:4 + packed.numel()].view(packed.shape)
+    shifted.copy_(packed)
+    y = q.qmm_gemv(x, shifted, bits, 128, scales, None, prob.zero_const)
+    assert rel_err(y_to_f64(y), oracle_y(prob)) <= REL_TOL
+    assert q.qmm_device_status() == 0
