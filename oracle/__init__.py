@@ -86,6 +86,10 @@ def _load():
             lib.oracle_threads.restype = I
             lib.oracle_quantize_act.argtypes = [P, P, P, L, L]
             lib.oracle_quantize_act.restype = None
+            lib.oracle_interleave4.argtypes = [P, P, L, L]
+            lib.oracle_interleave4.restype = None
+            lib.oracle_deinterleave4.argtypes = [P, P, L, L]
+            lib.oracle_deinterleave4.restype = None
             _lib = lib
     return _lib
 
@@ -268,6 +272,29 @@ def qmm_signed(x_f64: np.ndarray, packed: np.ndarray, bits: int, group: int, sca
     table = np.array([lib.oracle_signed_value(c, bits) for c in range(1 << bits)], dtype=np.float64)
     w = table[codes] * np.repeat(_c(scales, np.float64), group, axis=1)
     return _c(x_f64, np.float64) @ w.T
+
+
+def interleave4(codes: np.ndarray) -> np.ndarray:
+    """uint8 codes [N][K] (4-bit, K % 8 == 0) -> the lane-interleaved layout
+    uint8 [N][K/2]: per 32-bit word, nibble slots hold codes 0 4 1 5 2 6 3 7."""
+    codes = _c(codes, np.uint8)
+    N, K = codes.shape
+    if K % 8:
+        raise ValueError("K must be a multiple of 8")
+    out = np.empty((N, K // 2), dtype=np.uint8)
+    _load().oracle_interleave4(_ptr(codes), _ptr(out), N, K)
+    return out
+
+
+def deinterleave4(packed: np.ndarray, K: int) -> np.ndarray:
+    """Inverse of interleave4: uint8 [N][K/2] -> codes uint8 [N][K]."""
+    packed = _c(packed, np.uint8)
+    N = packed.shape[0]
+    if K % 8 or packed.shape[1] * 2 != K:
+        raise ValueError("packed row length must be K/2, K a multiple of 8")
+    out = np.empty((N, K), dtype=np.uint8)
+    _load().oracle_deinterleave4(_ptr(packed), _ptr(out), N, K)
+    return out
 
 
 def float_value(code: int, ebits: int, mbits: int) -> float:

@@ -46,6 +46,14 @@
  *     q = 0 for a token whose stored scale is 0.  The quotients that decide
  *     the integers are single-precision IEEE divisions (the precision the
  *     GPU kernel uses too).
+ *  8. Lane-interleaved int4 layout (BitLLM sec. 4.3, Fig. 6 and Fig. 8(b)):
+ *     eight 4-bit codes per 32-bit little-endian word, with nibble slot s
+ *     at bits [4s, 4s+4); slot 2j holds code j and slot 2j+1 code j+4 of the
+ *     word's eight (j = 0..3), so the slots read 0 4 1 5 2 6 3 7, the order
+ *     Fig. 6 prints.  Then the bytes of W & 0x0F0F0F0F are codes 0..3 and
+ *     the bytes of (W & 0xF0F0F0F0) >> 4 are codes 4..7: one shift and two
+ *     masks give four byte-aligned values each (Fig. 8(b); the page prints
+ *     the first mask garbled as 0xF0F0F0F0 for both halves).
  *
  * Every function follows the definition directly: per-bit loops, no word
  * tricks, no blocking.
@@ -337,4 +345,33 @@ double oracle_float_value(int code, int ebits, int mbits)
     else
         v = ldexp((double)M / (double)(1 << mbits), 1 - bias);
     return sign ? -v : v;
+}
+
+/* ---- 8. lane-interleaved int4 layout ------------------------------------ */
+
+/* The nibble slot (0..7) of code r (0..7) within its 32-bit word. */
+static int interleave4_slot(int r) { return r < 4 ? 2 * r : 2 * (r - 4) + 1; }
+
+void oracle_interleave4(const uint8_t *codes, uint8_t *out, long N, long K)
+{
+    for (long n = 0; n < N; ++n) {
+        const uint8_t *c = codes + n * K;
+        uint8_t *row = out + n * (K / 2);
+        memset(row, 0, (size_t)(K / 2));
+        for (long k = 0; k < K; ++k) {
+            const long slot = 8 * (k / 8) + interleave4_slot((int)(k % 8));
+            row[slot / 2] |= (uint8_t)((c[k] & 15u) << (4 * (slot % 2)));
+        }
+    }
+}
+
+void oracle_deinterleave4(const uint8_t *in, uint8_t *codes, long N, long K)
+{
+    for (long n = 0; n < N; ++n) {
+        const uint8_t *row = in + n * (K / 2);
+        for (long k = 0; k < K; ++k) {
+            const long slot = 8 * (k / 8) + interleave4_slot((int)(k % 8));
+            codes[n * K + k] = (uint8_t)((row[slot / 2] >> (4 * (slot % 2))) & 15u);
+        }
+    }
 }

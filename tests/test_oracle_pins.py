@@ -423,3 +423,47 @@ def test_float_matmul_brute_force(e, m):
             exact = sum(Fraction(float(x[mm, k])) * _float_fraction(int(codes[n, k]), e, m)
                         * Fraction(float(s[n, k // G])) for k in range(K))
             assert abs(y[mm, n] - float(exact)) <= 1e-12 * max(1.0, abs(float(exact)))
+
+
+# ---- lane-interleaved int4 layout (BitLLM Fig. 6, sec. 4.3 Fig. 8(b)) ----------------
+def _nibble_slots(packed_row):
+    """The nibble slots of a byte row, slot 0 = low nibble of byte 0 upwards."""
+    return [(int(b) >> (4 * h)) & 15 for b in packed_row for h in (0, 1)]
+
+
+def test_interleave4_matches_the_printed_order():
+    (line,) = list(_golden_lines("lane_interleave_order.txt"))
+    pos_in = [int(v) for v in line[0].split()]
+    pos_stored = [int(v) for v in line[1].split()]
+    assert pos_in == list(range(32)) and sorted(pos_stored) == pos_in
+    # codes 0..15 twice: each value names its position modulo 16
+    codes = (np.arange(32) % 16).astype(np.uint8).reshape(1, 32)
+    slots = _nibble_slots(oracle.interleave4(codes)[0])
+    assert slots == [p % 16 for p in pos_stored]
+
+
+def test_interleave4_one_shift_two_masks_give_byte_aligned_codes():
+    st = synthetic.SplitMix64(2024)
+    codes = st.uniform_bits(5 * 64, 4).reshape(5, 64)
+    words = oracle.interleave4(codes).view("<u4")
+    for n in range(5):
+        for w, W in enumerate(words[n]):
+            W = int(W)
+            lo = [(W & 0x0F0F0F0F) >> (8 * i) & 0xFF for i in range(4)]
+            hi = [((W & 0xF0F0F0F0) >> 4) >> (8 * i) & 0xFF for i in range(4)]
+            assert lo == list(codes[n, 8 * w:8 * w + 4])
+            assert hi == list(codes[n, 8 * w + 4:8 * w + 8])
+
+
+def test_interleave4_is_the_canonical_pack_of_permuted_codes_and_inverts():
+    st = synthetic.SplitMix64(77)
+    codes = st.uniform_bits(3 * 136, 4).reshape(3, 136)
+    order = np.array([0, 4, 1, 5, 2, 6, 3, 7])
+    perm = (np.arange(136) // 8 * 8)[:, None].reshape(-1)
+    perm = perm + np.tile(order, 136 // 8)
+    canonical, _ = oracle.pack(codes[:, perm], 4)
+    inter = oracle.interleave4(codes)
+    np.testing.assert_array_equal(inter, canonical)
+    np.testing.assert_array_equal(oracle.deinterleave4(inter, 136), codes)
+    with pytest.raises(ValueError):
+        oracle.interleave4(codes[:, :12])
