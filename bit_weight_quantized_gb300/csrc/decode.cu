@@ -13,15 +13,15 @@
 //
 // Work split.  CTA c owns at most 32 consecutive columns (two 16-row MMA
 // tiles); warp w owns K/8 codes of all of them, in blocks of 64.  In a block,
-// quad thread t owns codes [16t, 16t + 16) of each of its rows (b/2 words,
-// rounded up, read straight from global memory: one 8-byte load at b = 4, one
-// 16-byte load at b = 8), and the MMA's k order is
-// permuted to match: the 16 codes of MMA step s of thread t are its codes
-// 4s .. 4s + 3, so the B fragment is x[16t + 4s .. 16t + 4s + 3] of the block,
-// one 32-byte load per thread and block.  No activation staging, no shared
-// memory before the final reduction, one CTA barrier.  Loads run one block
-// ahead in registers; before waiting for the preceding kernel the weights are
-// prefetched into L2 (the weights are not that kernel's output).
+// quad thread t owns codes [16t, 16t + 16) of each of its rows: b/2 words,
+// rounded up, read straight from global memory (one 8-byte load at b = 4, one
+// 16-byte load at b = 8).  The MMA's k order is permuted to match: the 16
+// codes of MMA step s of thread t are its codes 4s .. 4s + 3, so the B fragment
+// is x[16t + 4s .. 16t + 4s + 3] of the block, one 32-byte load per thread and
+// block.  No activation staging, no shared memory before the final reduction,
+// one CTA barrier.  Loads run one block ahead in registers; before waiting for
+// the preceding kernel the weights are prefetched into L2 (the weights are not
+// that kernel's output).
 #include "common.cuh"
 #include "decode.h"
 
@@ -188,7 +188,8 @@ decode_kernel(const DecodeParams p)
                               xw[2 * s], xw[2 * s + 1]);
         }
         if (((j + 1) & group_end) == 0) {   // the end of a group
-            float X = xsum;                   // this quad's token, all 16 t-parts
+            // X_g of the quad's token: the sum of its four threads' 16-code slices of x
+            float X = xsum;
             X += __shfl_xor_sync(0xffffffffu, X, 1);
             X += __shfl_xor_sync(0xffffffffu, X, 2);
             // the accumulator columns are tokens 2t and 2t + 1 (lanes 4 (2t), 4 (2t + 1))
