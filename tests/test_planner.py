@@ -6,6 +6,10 @@ every row and every K chunk, keep the padded pitch that makes the MMA quads'
 reads conflict-free, lay out shared memory without overlap inside the per-CTA
 limit, and fit the decode shapes in half an SM (two CTAs per SM, so that
 consecutive calls overlap).
+
+tests/decode_route_check.cu does the same for the decode kernel's shape rule
+(bit_weight_quantized_gb300/csrc/decode.cu, decode_supports), checked against
+the rule as documented for qmm_gemv.
 """
 import json
 import os
@@ -114,3 +118,33 @@ def test_decode_shapes_fit_two_ctas_per_sm(plans):
     for p in plans:
         if p["M"] == 1 and p["N"] == 4096 and p["K"] == 4096:
             assert p["smem"] <= p["smem_pair"], (p["bits"], p["smem"])
+
+
+# ---- the decode kernel's shape rule (decode.cu) ------------------------------------
+def _decode_rule(M, N, K, G, sms):
+    """M <= 8, G in {64, 128}, K a positive multiple of 8 G, at most 32 columns per CTA
+    with min(N, SMs) CTAs."""
+    grid = min(N, sms)
+    return 1 <= M <= 8 and G in (64, 128) and K >= 8 * G and K % (8 * G) == 0 and -(-N // grid) <= 32
+
+
+def test_decode_route_rule(tmp_path):
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    exe = str(tmp_path / "decode_route_check")
+    subprocess.run([nvcc, "-std=c++17", "-O1", "-gencode", "arch=compute_103a,code=sm_103a",
+                    "--expt-relaxed-constexpr", "-o", exe, os.path.join(HERE, "decode_route_check.cu")],
+                   check=True, capture_output=True)
+    shapes = [(M, N, K, G, sms) for M in (0, 1, 8, 9, 16) for G in (32, 64, 128)
+              for K in (256, 512, 1024, 1536, 4096, 12288)
+              for N in (1, 151, 152, 4096, 4863, 4864, 4865, 14336)
+              for sms in (152, 148)]
+    stdin = "".join(" ".join(map(str, s)) + "\n" for s in shapes)
+    out = subprocess.run([exe], input=stdin, capture_output=True, text=True, check=True).stdout
+    rows = [tuple(map(int, line.split())) for line in out.splitlines()]
+    assert len(rows) == len(shapes)
+    for r in rows:
+        assert bool(r[5]) == _decode_rule(*r[:5]), r
+    # the decode sweep's shape takes the decode kernel, the skinny batch shapes do not
+    assert _decode_rule(1, 4096, 4096, 128, 152) and not _decode_rule(16, 14336, 4096, 64, 152)
