@@ -368,6 +368,11 @@ qmm_status qmm_gemm(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int
         return QMM_ERR_UNSUPPORTED;
     if (M == 0 || N == 0)
         return QMM_OK;
+    if (K > 0 && (!aligned(x, 16) || !aligned(packed, 16) || !aligned(y, 16) ||
+                  (static_cast<long long>(K) * bits / 8) % 16))
+        return QMM_ERR_ALIGN;
+    if (K > 0 && !gemm_supports_bits(bits))
+        return QMM_ERR_UNSUPPORTED;
     const DeviceFacts *f = device_facts();
     if (!f || f->usable != QMM_OK)
         return QMM_ERR_DEVICE;

@@ -4,7 +4,9 @@
 // TMA tile loads, packed fp16 arithmetic and the legacy tensor-core MMA.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "../../include/qmm.h"
@@ -129,7 +131,34 @@ __device__ __forceinline__ void prefetch_tmap(const void *tmap)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
-// ---- named barriers among a subset of warps -----------------------------------
+// ---- per-kernel dynamic shared-memory limit ------------------------------------
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) is per kernel and device.
+// Each kernel instantiation keeps one SmemLimit; the limit only grows, under a
+// mutex, so that concurrent host threads never launch with more dynamic shared
+// memory than the attribute already allows.
+struct SmemLimit {
+    std::atomic<int> bytes[64] = {};
+    std::mutex mu;
+};
+
+template <typename Kernel>
+cudaError_t ensure_smem_limit(SmemLimit &lim, Kernel kern, int smem)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    if (lim.bytes[dev].load(std::memory_order_acquire) >= smem)
+        return cudaSuccess;
+    std::lock_guard<std::mutex> g(lim.mu);
+    if (lim.bytes[dev].load(std::memory_order_relaxed) < smem) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess)
+            return e;
+        lim.bytes[dev].store(smem, std::memory_order_release);
+    }
+    return cudaSuccess;
+}
+
 // ---- packed fp16 arithmetic on raw 32-bit registers ----------------------------------
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t bits)
 {

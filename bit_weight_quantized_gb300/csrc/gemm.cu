@@ -76,6 +76,7 @@ struct GemmParams {
     int M, N, K, group, ng, zero_const, bf16;
     int group_log2;           // G = 1 << group_log2
     int vec_scales;           // scale rows 16-byte aligned and ng % 8 == 0 (zeros 8-byte aligned)
+    int zsplit;               // bf16 with zeros that may exceed 128: subtract z in two exact steps
     int tiles_n, mtiles, passes, ksteps;
 };
 
@@ -201,10 +202,15 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16)
 // scale is split s = s_hi + s_lo with both parts exact in bf16 (s_hi = the
 // scale rounded to 8 significant bits, s_lo = the remaining <= 4 bits), so that
 // (q - z) * s_lo is exact and one bf16 FMA rounds the exact product once.
+// bf16 holds every integer up to 256 but not the odd ones above, so 128 + z is
+// exact only for z <= 128.  For larger zeros the subtraction goes in two exact
+// steps: 128 + min(z, 128) first (leaving q - min(z, 128), at most 128 in
+// magnitude), then the rest z - 128 (the result |q - z| <= 255 is exact).
 struct GroupConst {
     uint32_t s2;      // fp16: s;  bf16: s_hi
     uint32_t slo2;    // bf16: s_lo
     uint32_t off2;
+    uint32_t zrest2;  // bf16 with zsplit: max(z - 128, 0), else 0
 };
 
 // Scales and zeros of eight consecutive groups 8w .. 8w + 7 of one column, held
@@ -266,10 +272,14 @@ __device__ __forceinline__ GroupConst group_const(uint16_t s_bits, uint8_t z, bo
     const float s = f16_bits_to_f32(s_bits);
     c.s2 = pack2(s, s, bf16);
     c.slo2 = 0;
+    c.zrest2 = 0;
     if (bf16) {
         const float s_hi = __uint_as_float((c.s2 & 0xFFFFu) << 16);
         const float s_lo = s - s_hi;                              // exact in fp32 and in bf16
         c.slo2 = pack2(s_lo, s_lo, true);
+        const float rest = static_cast<float>(z > 128 ? z - 128 : 0);
+        c.zrest2 = pack2(rest, rest, true);
+        z = z > 128 ? 128 : z;
     }
     const float off = (bf16 ? 128.f : 1024.f) + static_cast<float>(z);   // exact in 16 bits
     c.off2 = pack2(off, off, bf16);
@@ -280,7 +290,8 @@ __device__ __forceinline__ GroupConst group_const(uint16_t s_bits, uint8_t z, bo
 // each (q - z) * s.  A byte permute puts code 2j in the low half and code 2j+1
 // (pre-shifted by 4) in the high half; a LOP3 sets the exponent so each half
 // reads 2^E + q; the subtraction is exact and the scaling rounds once.
-__device__ __forceinline__ void dequant_word4(uint32_t w, const GroupConst &c, bool bf16, uint32_t (&o)[4])
+__device__ __forceinline__ void dequant_word4(uint32_t w, const GroupConst &c, bool bf16, bool zsplit,
+                                              uint32_t (&o)[4])
 {
     const uint32_t hi = w >> 4;
     const uint32_t magic = bf16 ? 0x43004300u : 0x64006400u;   // 128.0 / 1024.0
@@ -289,7 +300,9 @@ __device__ __forceinline__ void dequant_word4(uint32_t w, const GroupConst &c, b
         const uint32_t sel = static_cast<uint32_t>(j) | (static_cast<uint32_t>(4 + j) << 8);
         const uint32_t t = prmt(w, hi, sel);
         const uint32_t v = lop3_and_or(t, 0x000F000Fu, magic);
-        const uint32_t qz = sub2(v, c.off2, bf16);                 // q - z, exact
+        uint32_t qz = sub2(v, c.off2, bf16);                       // q - min(z, 128), exact
+        if (zsplit)
+            qz = sub2(qz, c.zrest2, true);                         // q - z, exact
         if (bf16)
             o[j] = fma2_bf16(qz, c.s2, mul2(qz, c.slo2, true));     // one rounding of (q - z) * s
         else
@@ -329,6 +342,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUt
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const bool bf16 = p.bf16 != 0;
+    const bool zsplit = p.zsplit != 0;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kXStages; ++i)
@@ -506,7 +520,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUt
 #pragma unroll
                             for (int i = 0; i < kDeqWords; ++i) {
                                 uint32_t o[4];
-                                dequant_word4(wv[i], gc, bf16, o);
+                                dequant_word4(wv[i], gc, bf16, zsplit, o);
                                 *reinterpret_cast<uint4 *>(brow + (((qd * kDeqWords + i) ^ (r & 7)) << 4)) =
                                     make_uint4(o[0], o[1], o[2], o[3]);
                             }
@@ -587,15 +601,9 @@ qmm_status launch_gemm(const CUtensorMap &tmx, const CUtensorMap &tmw, GemmParam
     if (smem_optin < smem)
         return QMM_ERR_UNSUPPORTED;
     p.passes = (p.mtiles + MT - 1) / MT;
-    static int configured[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-        if (cudaFuncSetAttribute(gemm_kernel<MT, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess)
-            return QMM_ERR_CUDA;
-        configured[dev] = 1;
-    }
+    static SmemLimit limit;
+    if (ensure_smem_limit(limit, gemm_kernel<MT, S>, smem) != cudaSuccess)
+        return QMM_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
@@ -612,6 +620,8 @@ qmm_status launch_gemm(const CUtensorMap &tmx, const CUtensorMap &tmw, GemmParam
 }
 
 }  // namespace
+
+bool gemm_supports_bits(int bits) { return bits == 4; }
 
 qmm_status gemm_dispatch(const void *x, bool x_bf16, const uint8_t *packed, int bits, int group,
                          const void *scales, const uint8_t *zeros, int zero_const, void *y, int M,
@@ -646,6 +656,7 @@ qmm_status gemm_dispatch(const void *x, bool x_bf16, const uint8_t *packed, int 
     p.ng = K / group;
     p.zero_const = zeros ? 0 : zero_const;
     p.bf16 = x_bf16 ? 1 : 0;
+    p.zsplit = x_bf16 && (zeros || zero_const > 128) ? 1 : 0;
     p.group_log2 = group == 32 ? 5 : group == 64 ? 6 : 7;
     p.vec_scales = reinterpret_cast<uintptr_t>(scales) % 16 == 0 && p.ng % 8 == 0 &&
                    (!zeros || reinterpret_cast<uintptr_t>(zeros) % 8 == 0);

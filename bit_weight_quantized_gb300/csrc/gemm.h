@@ -10,6 +10,9 @@
 
 namespace qmm {
 
+// Widths the tiled kernel dequantizes.
+bool gemm_supports_bits(int bits);
+
 qmm_status gemm_dispatch(const void *x, bool x_bf16, const uint8_t *packed, int bits, int group,
                          const void *scales, const uint8_t *zeros, int zero_const, void *y, int M,
                          int N, int K, int *status, int num_sms, int smem_optin,

@@ -818,17 +818,9 @@ template <int B, int NT, int R, int MODE>
 cudaError_t launch_skinny(const GemvParams &p, int grid, int smem, cudaStream_t stream)
 {
     auto kern = skinny_kernel<B, NT, R, MODE>;
-    static int configured[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64)
-        return cudaErrorInvalidDevice;
-    if (configured[dev] < smem) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess)
-            return e;
-        configured[dev] = smem;
-    }
+    static SmemLimit limit;
+    if (const cudaError_t e = ensure_smem_limit(limit, kern, smem); e != cudaSuccess)
+        return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);

@@ -35,17 +35,21 @@
  *    outputs unspecified and returns; qmm_device_status() reports and clears
  *    it.  Nothing in the library aborts, throws across the ABI or traps.
  *  - Outputs are written with round-to-nearest-even from fp32.
- *  - Overlap of consecutive calls.  qmm_gemv, qmm_gemm and qmm_w4a8 launch
- *    with programmatic dependent launch: a call's kernel may start while the
- *    previous kernel on the stream is still running, and it may read the weight
- *    arguments (packed / w4, scales / ws, zeros) BEFORE it waits for that
- *    kernel; activations are read only after the wait.  So the weight
- *    arguments of a call must not be written by the kernel that directly
- *    precedes it on the stream if that kernel is itself a qmm_gemv, qmm_gemm
- *    or qmm_w4a8 call (for example as its y).  Kernels that do not opt in to
- *    early launch (qmm_pack, and ordinary CUDA / PyTorch kernels) complete
- *    before the call's kernel starts, so writing the weights with them is
- *    fine.
+ *  - Overlap of consecutive calls.  qmm_gemv, qmm_gemm, qmm_w4a8, qmm_w8a8,
+ *    qmm_gemv_float and qmm_quantize_act launch with programmatic dependent
+ *    launch and let the next kernel on the stream start as soon as they start
+ *    themselves.  The matmul calls read their weight arguments (packed / w4 /
+ *    w8, scales / ws, zeros) BEFORE they wait for the preceding kernel;
+ *    activations (x / xq, sa) are read only after that wait, which returns
+ *    once every earlier kernel on the stream has completed.  Because each of
+ *    these calls lets its successor start early, a whole run of consecutive
+ *    such calls on one stream can be in flight at once.  So no call of such a
+ *    run may write the weight arguments of a later call of the same run (for
+ *    example as its y).  Any other work on the stream ends the run: qmm_pack,
+ *    qmm_unpack, qmm_flip_sign, copies and ordinary CUDA / PyTorch kernels do
+ *    not opt in to early launch, so the calls after them start only once they
+ *    (and everything before them) have completed, and writing weights with
+ *    them is fine.
  */
 #ifndef QMM_H_
 #define QMM_H_
@@ -135,10 +139,16 @@ QMM_API qmm_status qmm_set_gemv_kernel(int kernel);
 
 /* Tiled matmul for M >= 17 (the dense-contraction regime, Tilus review
  * supporting_citations [41]: tensor-core instruction layouts).  Same
- * arguments and storage as qmm_gemv; activations and outputs may be
- * QMM_BF16 or QMM_F16 (x_dtype == y_dtype).  Weights are dequantized to
- * bf16/fp16 (q - z) * s tiles in shared memory and multiplied with
- * tcgen05 MMAs accumulating in fp32 in tensor memory. */
+ * arguments and storage as qmm_gemv, with these differences:
+ *   - x and y may be QMM_BF16 or QMM_F16 (x_dtype == y_dtype);
+ *   - x, y and packed must be 16-byte aligned and K * bits / 8 (the packed
+ *     row pitch) a multiple of 16 bytes (else QMM_ERR_ALIGN);
+ *   - bits must be 4 (else QMM_ERR_UNSUPPORTED).
+ * Weights are dequantized to bf16/fp16 (q - z) * s tiles in shared memory
+ * (one rounding of the exact product; q - z itself is exact for every zero
+ * 0..255) and multiplied with tcgen05 MMAs accumulating in fp32 in tensor
+ * memory.  With fp16 the dequantized weight must be finite in fp16:
+ * |q - z| * s < 65504. */
 QMM_API qmm_status qmm_gemm(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int bits,
                     int group, const void *scales, const uint8_t *zeros, int zero_const,
                     void *y, qmm_dtype y_dtype, int M, int N, int K, cudaStream_t stream);

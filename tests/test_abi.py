@@ -87,6 +87,11 @@ def test_empty_problems_are_noops(lib):
 def test_gemm_and_w4a8_argument_errors(lib):
     assert lib.qmm_gemm(A16, 1, B16, 4, 128, A16, None, 8, B16, 1, 8, 64, 128, None) == 3
     assert lib.qmm_gemm(A16, 1, B16, 4, 128, A16, None, 8, B16, 0, 64, 64, 128, None) == 5
+    # the tiled path needs 16-byte aligned x, y and packed, and a packed row
+    # pitch (K * bits / 8 bytes) that is a multiple of 16
+    assert lib.qmm_gemm(A16, 1, B16, 4, 128, A16, None, 8, _fake(0x20002), 1, 64, 64, 128, None) == 4
+    assert lib.qmm_gemm(A16, 1, _fake(0x20004), 4, 128, A16, None, 8, B16, 1, 64, 64, 128, None) == 4
+    assert lib.qmm_gemm(A16, 1, B16, 3, 32, A16, None, 4, B16, 1, 64, 64, 96, None) == 4
     assert lib.qmm_w4a8(A16, A16, B16, A16, 100, B16, None, 1, 64, 128, None) == 3
     assert lib.qmm_w4a8(A16, A16, B16, A16, 128, B16, None, 65, 64, 128, None) == 3
     assert lib.qmm_w4a8(None, A16, B16, A16, 128, B16, None, 1, 64, 128, None) == 1
