@@ -166,16 +166,39 @@ class W4A8Problem:
         return 2 * self.M * self.N * self.K
 
 
+X_LAWS = ("normal", "shift2", "shift8", "abs4", "outlier")
+
+
 def make_qmm(M: int, N: int, K: int, bits: int, group: int, *, zero_mode: str,
              x_dtype: str = "f16", y_dtype: str = "f16", seed: int = 0,
-             label: str = "") -> QmmProblem:
+             label: str = "", x_law: str = "normal", code_fill: Optional[str] = None,
+             scale_mult: float = 1.0) -> QmmProblem:
     """Draw one instance.
 
     zero_mode: "const8" (z = 8), "half" (z = 2**(bits-1)), "group" (uint8 per
-    group, uniform on [0, 2**bits)), or "none" (z = 0).
+    group, uniform on [0, 2**bits)), "none" (z = 0), "top" (z = 2**bits - 1)
+    or "max" (z = 255, the largest stored zero).
+
+    x_law (the activation law, N(0,1) unless stated):
+      "normal"   N(0, 1)
+      "shift2"   N(2, 1)        mean-shifted activations
+      "shift8"   N(8, 1)
+      "abs4"     4 |N(0, 1)|    non-negative, SiLU-like
+      "outlier"  N(0, 1) with 8 channels (drawn after the activations, the
+                 same channels for every token) multiplied by 100
+    code_fill: None (codes drawn), "max" (every code 2**bits - 1) or "min"
+    (every code 0); the codes are drawn either way, so the rest of the
+    stream is unchanged.
+    scale_mult multiplies the drawn fp16 scales (a power of two keeps them exact).
     """
     st = SplitMix64(seed)
     codes = st.uniform_bits(N * K, bits).reshape(N, K)
+    if code_fill == "max":
+        codes[:] = (1 << bits) - 1
+    elif code_fill == "min":
+        codes[:] = 0
+    elif code_fill is not None:
+        raise ValueError(code_fill)
     ng = K // group
     zeros = None
     if zero_mode == "const8":
@@ -184,13 +207,30 @@ def make_qmm(M: int, N: int, K: int, bits: int, group: int, *, zero_mode: str,
         zc = 1 << (bits - 1)
     elif zero_mode == "none":
         zc = 0
+    elif zero_mode == "top":
+        zc = (1 << bits) - 1
+    elif zero_mode == "max":
+        zc = 255
     elif zero_mode == "group":
         zc = 0
         zeros = st.uniform_bits(N * ng, bits).reshape(N, ng)
     else:
         raise ValueError(zero_mode)
     scales = scale_law(st, N * ng).reshape(N, ng)
+    if scale_mult != 1.0:
+        scales = (scales.astype(np.float64) * scale_mult).astype(np.float16)
     xn = st.normal(M * K).reshape(M, K)
+    if x_law == "shift2":
+        xn = xn + 2.0
+    elif x_law == "shift8":
+        xn = xn + 8.0
+    elif x_law == "abs4":
+        xn = 4.0 * np.abs(xn)
+    elif x_law == "outlier":
+        ch = (st.next(8) % np.uint64(K)).astype(np.int64)
+        xn[:, ch] *= 100.0
+    elif x_law != "normal":
+        raise ValueError(x_law)
     if x_dtype == "f16":
         x = xn.astype(np.float16)
     elif x_dtype == "bf16":
