@@ -265,22 +265,40 @@ def test_act_quant_worked_examples(case):
     assert q[0].tolist() == [int(v) for v in qs]
 
 
-def test_act_quant_matches_ieee_single_precision():
-    # the scale and the quotients are IEEE single-precision divisions rounded to
-    # fp16 / to the nearest integer (ties to even): numpy's float32 arithmetic
-    # and rint implement the same IEEE operations independently of the C code
-    rng = np.random.default_rng(7)
-    rows = [rng.standard_normal(512) * m for m in (1e-6, 3e-3, 1.0, 40.0, 1e4)]
-    rows.append(np.where(rng.random(512) < 0.5, 0.5, -0.5) * 127.0 / 64.0)   # exact ties
-    x = np.array(rows, dtype=np.float16)
-    q, sa = oracle.quantize_act(x.view(np.uint16))
-    x32 = x.astype(np.float32)
-    amax = np.max(np.abs(x32), axis=1)
-    s_ref = (amax / np.float32(127)).astype(np.float16)
-    np.testing.assert_array_equal(sa, s_ref.view(np.uint16))
-    s32 = s_ref.astype(np.float32)[:, None]
-    q_ref = np.where(s32 > 0, np.clip(np.rint(x32 / np.where(s32 > 0, s32, 1)), -128, 127), 0)
-    np.testing.assert_array_equal(q, q_ref.astype(np.int8))
+def _f16_round_exact(v):
+    """Round a non-negative Fraction to the nearest fp16 value, ties to even,
+    in exact rational arithmetic (normal and subnormal ranges; no overflow)."""
+    from fractions import Fraction
+    if v == 0:
+        return Fraction(0)
+    e = v.numerator.bit_length() - v.denominator.bit_length()
+    if Fraction(2) ** e > v:
+        e -= 1                                   # now 2^e <= v < 2^(e+1)
+    ulp = Fraction(2) ** (max(e, -14) - 10)      # 11 significant bits; subnormal ulp 2^-24
+    return round(v / ulp) * ulp                  # Fraction.__round__ ties to even
+
+
+@pytest.mark.parametrize("amax", [127.0, 12.7, 0.75, 1000.0, 3e-3, 60000.0, 1e-6])
+def test_act_quant_equals_exact_rational_rounding_on_every_fp16(amax):
+    # Eq. (1) read in exact arithmetic: s = fp16(max|x| / 127) and q = round(x / s),
+    # both rounded once, ties to even, from the exact rational values.  The oracle
+    # divides in IEEE single precision; this checks, for one token per amax that
+    # holds EVERY finite fp16 value of magnitude <= amax, that no such division
+    # ever decides a code (or the scale) differently from exact arithmetic.
+    from fractions import Fraction
+    a16 = np.float16(amax)
+    bits = np.arange(0, 0x7C00, dtype=np.uint16)
+    mags = bits.view(np.float16)
+    mags = mags[mags <= a16]
+    vals = np.concatenate([mags, -mags[1:], [a16]]).astype(np.float16)
+    pad = (-vals.size) % 8
+    vals = np.concatenate([vals, np.zeros(pad, dtype=np.float16)])
+    q, sa = oracle.quantize_act(vals.reshape(1, -1).view(np.uint16))
+    s = _f16_round_exact(Fraction(float(a16)) / 127)
+    assert Fraction(float(sa.view(np.float16)[0])) == s
+    # a scale that rounds to 0 (max|x| below about 127 x 2^-25) quantizes to 0
+    want = [round(Fraction(float(v)) / s) if s else 0 for v in vals]
+    assert q[0].tolist() == want
 
 
 def test_act_quant_error_bound_and_range():
