@@ -13,8 +13,10 @@ Timing: the step's launches are captured once in a CUDA graph per input copy
 the inputs rotate over copies whose total exceeds twice the L2, so every step
 reads its weights from HBM.  W warm-up steps, then exactly K timed steps
 between a barrier + synchronize on both sides, CUDA events on the launching
-stream, max over ranks.  Kernel durations for the roofline come from a second
-replay of the same launches with timing events between them.
+stream, max over ranks.  The step consists of the eight decode-kernel launches
+and nothing else, so the roofline's average launch duration is the timed step
+divided by eight; per-width figures come from graphs of one width alone over
+weight copies that also exceed twice the L2.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -261,9 +263,9 @@ def run_reference(args, world, rank):
 
 
 
-def time_graph(torch, stream, launches, reps: int = 10):
+def time_graph(torch, stream, launches, reps: int = 10, sleep: bool = True):
     """Per-launch device time (ms) of `launches` (closures) captured in one CUDA
-    graph and replayed `reps` times; inputs rotate inside `launches`."""
+    graph and replayed `reps` times on `stream`; inputs rotate inside `launches`."""
     with torch.cuda.stream(stream):
         for f in launches:
             f()
@@ -272,9 +274,11 @@ def time_graph(torch, stream, launches, reps: int = 10):
     with torch.cuda.graph(g, stream=stream):
         for f in launches:
             f()
-    g.replay()
+    with torch.cuda.stream(stream):
+        g.replay()
     stream.synchronize()
-    time.sleep(0.2)   # timed as a kernel alone: the burst peak applies
+    if sleep:
+        time.sleep(0.2)   # timed as a kernel alone: the burst peak applies
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         a.record(stream)
@@ -285,7 +289,7 @@ def time_graph(torch, stream, launches, reps: int = 10):
     return a.elapsed_time(b) / (reps * len(launches))
 
 
-def measure_others(torch, q, dev, stream, peak_gbs, peak_tf, gemv_kernel="auto"):
+def measure_others(torch, q, dev, stream, peak_gbs, peak_tf, gemv_kernel="auto", l2=136 << 20):
     """The other workload families, timed the same way on device-generated
     inputs of the workloads' shapes and laws (the values do not change the
     work): skinny decode (M = 16, N = 14336, b = 6, group 64), the decode
@@ -295,6 +299,12 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf, gemv_kernel="auto")
     per-token int8 quantizer), W8A8 (the same shapes, group 32), float6 e3m2
     weights (M = 1, K = N = 4096) and the quantizer alone (K = 4096)."""
     out = {}
+
+    def ncopies(nbytes):
+        # distinct weight copies whose total exceeds twice the L2: every launch
+        # reads its weights from HBM
+        return -(-2 * l2 // nbytes) + 1
+
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
 
@@ -306,7 +316,8 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf, gemv_kernel="auto")
 
     # skinny: M=16, N=14336, b=6, group 64, uint8 zeros
     M, N, K, b, G = 16, 14336, 4096, 6, 64
-    sets = [(q.qmm_pack(codes(N, K, b), b), scales(N, K // G), codes(N, K // G, b)) for _ in range(4)]
+    sets = [(q.qmm_pack(codes(N, K, b), b), scales(N, K // G), codes(N, K // G, b))
+            for _ in range(ncopies(N * K * b // 8))]
     x = torch.randn(M, K, device=dev, generator=gen).half()
     y = torch.empty(M, N, dtype=torch.float16, device=dev)
     ms = time_graph(torch, stream, [lambda s=s_: q.qmm_gemv(x, s[0], b, G, s[1], s[2], out=y) for s_ in sets])
@@ -317,7 +328,7 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf, gemv_kernel="auto")
     # the decode kernel beside the skinny kernel (forced) on the decode shape
     # K = N = 4096, b = 4, group 128, M = 1 and 8
     N, K, b, G = 4096, 4096, 4, 128
-    sets = [(q.qmm_pack(codes(N, K, b), b), scales(N, K // G)) for _ in range(24)]
+    sets = [(q.qmm_pack(codes(N, K, b), b), scales(N, K // G)) for _ in range(ncopies(N * K * b // 8))]
     for M in (1, 8):
         x = torch.randn(M, K, device=dev, generator=gen).half()
         y = torch.empty(M, N, dtype=torch.float16, device=dev)
@@ -335,7 +346,7 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf, gemv_kernel="auto")
     del sets
     # tiled: K=8192, N=28672, int4 group 128, z=8, bf16
     N, K = 28672, 8192
-    wsets = [(q.qmm_pack(codes(N, K, 4), 4), scales(N, K // 128)) for _ in range(2)]
+    wsets = [(q.qmm_pack(codes(N, K, 4), 4), scales(N, K // 128)) for _ in range(ncopies(N * K // 2))]
     for M in (128, 512, 2048):
         x = torch.randn(M, K, device=dev, generator=gen).bfloat16()
         y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
@@ -347,7 +358,7 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf, gemv_kernel="auto")
     del wsets
     # W4A8: K=N=4096, group 128
     N = K = 4096
-    wsets = [(q.qmm_pack(codes(N, K, 4), 4), scales(N, K // 128)) for _ in range(8)]
+    wsets = [(q.qmm_pack(codes(N, K, 4), 4), scales(N, K // 128)) for _ in range(ncopies(N * K // 2))]
     for M in (1, 16, 64):
         xq = torch.randint(-127, 128, (M, K), dtype=torch.int8, device=dev, generator=gen)
         sa = (0.02 * torch.randn(M, device=dev, generator=gen).abs() + 1e-3).half()
@@ -370,7 +381,7 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf, gemv_kernel="auto")
     del wsets
     # W8A8: K = N = 4096, int8 weights, group 32 (the pages' W8A8 setting)
     wsets = [(torch.randint(-128, 128, (N, K), dtype=torch.int8, device=dev, generator=gen),
-              scales(N, K // 32)) for _ in range(8)]
+              scales(N, K // 32)) for _ in range(ncopies(N * K))]
     for M in (1, 16, 64):
         xq = torch.randint(-127, 128, (M, K), dtype=torch.int8, device=dev, generator=gen)
         sa = (0.02 * torch.randn(M, device=dev, generator=gen).abs() + 1e-3).half()
@@ -382,7 +393,7 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf, gemv_kernel="auto")
                                  "TOPs": round(2.0 * M * N * K / ms / 1e9, 1)}
     del wsets
     # float weights: float6 e3m2 (FP6-like), M = 1, K = N = 4096, group 128
-    fsets = [(q.qmm_pack(codes(N, K, 6), 6), scales(N, K // 128)) for _ in range(8)]
+    fsets = [(q.qmm_pack(codes(N, K, 6), 6), scales(N, K // 128)) for _ in range(ncopies(N * K * 6 // 8))]
     x = torch.randn(1, K, device=dev, generator=gen).half()
     y = torch.empty(1, N, dtype=torch.float16, device=dev)
     ms = time_graph(torch, stream, [lambda w=w_: q.qmm_gemv_float(x, w[0], 3, 2, 128, w[1], out=y) for w_ in fsets])
@@ -459,26 +470,6 @@ def run_ours(args, world, rank, local):
     with torch.cuda.graph(gA, stream=stream):
         for c in range(copies):
             step(c)
-    # graph B: same launches with timing events around each kernel
-    cu = _libcuda()
-    cu.cuEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
-    nev = 2 * len(probs)
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(copies)]
-    for row in events:          # torch creates the CUDA event at its first record
-        for ev in row:
-            ev.record(stream)
-    stream.synchronize()
-    gB = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gB, stream=stream):
-        cs = torch.cuda.current_stream()
-        for c in range(copies):
-            def mark(j, c=c):
-                r = cu.cuEventRecordWithFlags(ctypes.c_void_p(events[c][j].cuda_event),
-                                              ctypes.c_void_p(cs.cuda_stream), 1)
-                if r != 0:
-                    raise RuntimeError(f"cuEventRecordWithFlags failed ({r})")
-            step(c, mark)
-
     reps = max(1, args.steps // copies)
     steps = reps * copies
     warm_reps = max(1, -(-args.warmup // copies))
@@ -506,46 +497,20 @@ def run_ours(args, world, rank, local):
     total_bytes = sum_over_ranks(world, step_bytes * steps)
     value = total_bytes / (ms_max * 1e-3) / 1e9
 
-    # per-kernel durations (graph B), several replays; the events were recorded
-    # by graph nodes, so they are read through the driver API
-    cu.cuEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p,
-                                      ctypes.c_void_p]
+    # per-width durations: for each width a graph of back-to-back launches of
+    # that width alone, over distinct weight copies whose total exceeds twice
+    # the L2 (HBM-cold like the headline), replayed under CUDA events on `stream`
     kdur = np.zeros(len(probs))
-    nrep_b = max(4, min(64, reps))
-    how = "timing events between the launches inside the replayed graph"
-    try:
-        for _ in range(nrep_b):
-            gB.replay()
-            stream.synchronize()
-            for c in range(copies):
-                for i in range(len(probs)):
-                    f = ctypes.c_float()
-                    r = cu.cuEventElapsedTime(ctypes.byref(f),
-                                              ctypes.c_void_p(events[c][2 * i].cuda_event),
-                                              ctypes.c_void_p(events[c][2 * i + 1].cuda_event))
-                    if r != 0:
-                        raise RuntimeError(f"cuEventElapsedTime failed ({r})")
-                    kdur[i] += f.value
-        kdur /= nrep_b * copies          # ms per launch, per width
-    except RuntimeError as exc:
-        # fall back: a graph of 16 back-to-back launches per width, timed as a whole
-        how = f"per-width graphs of 16 launches timed as a whole ({exc})"
-        kdur[:] = 0
-        for i, p in enumerate(probs):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for r in range(16):
-                    pk, sc = sets[r % copies][i]
-                    q.qmm_gemv(xs[i], pk, p.bits, p.group, sc, None, p.zero_const, out=ys[i])
-            g.replay()
-            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                a.record(stream)
-                for _ in range(8):
-                    g.replay()
-                b_.record(stream)
-            stream.synchronize()
-            kdur[i] = a.elapsed_time(b_) / (8 * 16)
+    for i, p in enumerate(probs):
+        wb = p.N * p.K * p.bits // 8 + p.scales.size * 2
+        ncp = -(-2 * l2 // wb) + 1
+        wsets = [sets[c % copies][i] if c < copies else
+                 (sets[0][i][0].clone(), sets[0][i][1].clone()) for c in range(ncp)]
+        kdur[i] = time_graph(torch, stream,
+                             [lambda w=w_, p=p, i=i: q.qmm_gemv(xs[i], w[0], p.bits, p.group, w[1], None,
+                                                                p.zero_const, out=ys[i])
+                              for w_ in wsets], reps=8, sleep=False)
+        del wsets
     # isolated calls: each launch alone, after an L2 flush (a write of twice the
     # L2), timed by events around it; median and min of 50 per width
     flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.int32, device=dev)
@@ -572,7 +537,9 @@ def run_ours(args, world, rank, local):
         per_width[str(p.bits)] = {"us": round(kdur[i] * 1e3, 3), "GBps": round(gb, 1),
                                   "isolated_us_median": round(med, 2), "isolated_us_min": round(mn, 2)}
     peak, peak_kind = measured_peaks()
-    achieved = step_bytes / (kdur.sum() * 1e-3) / 1e9
+    # the timed step is nothing but the eight decode-kernel launches, back to back
+    # on `stream`: the kernel's average launch duration is ms_per_step / 8
+    achieved = step_bytes / (ms_max / steps * 1e-3) / 1e9
     for k in per_width:
         per_width[k]["frac"] = round(per_width[k]["GBps"] / peak, 4)
     traffic = profile_traffic() if args.gemv_kernel == "auto" else None
@@ -624,7 +591,7 @@ def run_ours(args, world, rank, local):
                 peak_tf = float(json.load(f)["bf16_tflops"])
         except Exception:
             peak_tf = 1900.0
-        others = measure_others(torch, q, dev, stream, peak, peak_tf, args.gemv_kernel)
+        others = measure_others(torch, q, dev, stream, peak, peak_tf, args.gemv_kernel, l2)
         assert q.qmm_device_status(stream) == 0
 
     cpu = None
@@ -653,10 +620,15 @@ def run_ours(args, world, rank, local):
                                     else "qmm::skinny_kernel<b,1,32,0> (b = 1..8)"),
                          "algorithmic_bytes_per_launch": round(step_bytes / len(probs)),
                          "frac_of_8TBs": round(achieved / 8000.0, 4),
-                         "duration_source": how,
-                         "per_width_note": "us / GBps: back-to-back launches (the roofline "
-                                           "durations); isolated_us_*: one launch after an L2 "
-                                           "flush, events around it, 50 runs"},
+                         "duration_source": ("CUDA events on the launching stream around the timed "
+                                             "region; the step is only the 8 decode launches (one "
+                                             "per width), so the average launch takes "
+                                             "ms_per_step / 8 and achieved equals value"),
+                         "per_width_note": "us / GBps: one width alone, back-to-back launches over "
+                                           "distinct weight copies totalling more than 2 x L2 "
+                                           "(HBM-cold), CUDA events around graph replays; "
+                                           "isolated_us_*: one launch after an L2 flush, events "
+                                           "around it, 50 runs"},
             "per_width": per_width,
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
