@@ -44,6 +44,7 @@ SIGNATURES = {
     "qmm_gemv_float": ([_P, _P, _I, _I, _I, _P, _P, _I, _I, _I, _P], _I),
     "qmm_quantize_act": ([_P, _P, _P, _I, _I, _P], _I),
     "qmm_set_gemv_kernel": ([_I], _I),
+    "qmm_gemv_route": ([_I, _I, _I, _I, _I, _I], _I),
     "qmm_device_status": ([_P], _I),
     "qmm_watchdog_selftest": ([_P], _I),
     "qmm_status_string": ([_I], ctypes.c_char_p),
@@ -182,6 +183,15 @@ def qmm_set_gemv_kernel(kernel: str):
     if kernel not in GEMV_KERNELS:
         raise ValueError(f"kernel must be one of {sorted(GEMV_KERNELS)}")
     _check(load().qmm_set_gemv_kernel(GEMV_KERNELS[kernel]), "qmm_set_gemv_kernel")
+
+
+def qmm_gemv_route(M: int, N: int, K: int, bits: int, group: int, stored_zeros: bool) -> str:
+    """The kernel a qmm_gemv call of this shape runs on the current device:
+    "decode" (the staged decode kernel) or "skinny"."""
+    r = load().qmm_gemv_route(M, N, K, bits, group, 1 if stored_zeros else 0)
+    if r < 0:
+        raise QmmError(-r, "qmm_gemv_route")
+    return "decode" if r == 0 else "skinny"
 
 
 def qmm_gemm(x, packed, bits, group, scales, zeros=None, zero_const=0, out=None,

@@ -294,8 +294,9 @@ qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int
         return QMM_ERR_DEVICE;
     if (K == 0)
         return from_cuda(cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * 2, stream));
+    DecodePlan plan;
     if (g_gemv_kernel.load(std::memory_order_relaxed) == QMM_GEMV_AUTO && aligned(packed, 16) &&
-        decode_supports(M, N, K, group, f->num_sms)) {
+        decode_plan(M, N, K, group, bits, zeros != nullptr, f->num_sms, f->smem_pair, f->smem_optin, &plan)) {
         DecodeParams d;
         std::memset(&d, 0, sizeof(d));
         d.x = static_cast<const uint16_t *>(x);
@@ -303,13 +304,16 @@ qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int
         d.scales = static_cast<const uint16_t *>(scales);
         d.zeros = zeros;
         d.y = y;
+        d.status = f->status;
+        d.row_bytes = static_cast<long long>(K) * bits / 8;
         d.M = M;
         d.N = N;
         d.K = K;
         d.group_log2 = group == 64 ? 6 : 7;
-        d.zero_const = zeros ? 0 : zero_const;
         d.y_bf16 = y_dtype == QMM_BF16;
-        return from_cuda(launch_decode(d, bits, f->num_sms, stream));
+        d.zero_const = zeros ? 0 : zero_const;
+        d.pl = plan;
+        return from_cuda(launch_decode(d, bits, stream));
     }
 
     GemvParams p;
@@ -345,6 +349,22 @@ qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int
     default: e = gemv_launch_w8(p, grid, smem, stream); break;
     }
     return from_cuda(e);
+}
+
+int qmm_gemv_route(int M, int N, int K, int bits, int group, int stored_zeros)
+{
+    if (M < 1 || M > 16 || N < 1 || K < 1 || bits < 1 || bits > 8 ||
+        (group != 32 && group != 64 && group != 128) || K % group)
+        return -static_cast<int>(QMM_ERR_SHAPE);
+    const DeviceFacts *f = device_facts();
+    if (!f || f->usable != QMM_OK)
+        return -static_cast<int>(QMM_ERR_DEVICE);
+    if (g_gemv_kernel.load(std::memory_order_relaxed) != QMM_GEMV_AUTO)
+        return QMM_GEMV_SKINNY;
+    DecodePlan plan;
+    return decode_plan(M, N, K, group, bits, stored_zeros != 0, f->num_sms, f->smem_pair, f->smem_optin, &plan)
+               ? QMM_GEMV_AUTO
+               : QMM_GEMV_SKINNY;
 }
 
 qmm_status qmm_set_gemv_kernel(int kernel)

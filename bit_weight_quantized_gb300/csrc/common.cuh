@@ -141,8 +141,13 @@ struct SmemLimit {
     std::mutex mu;
 };
 
+// With max_carveout the kernel also asks for the largest shared-memory share of
+// the SM's L1 / shared storage.  Kernels that run back to back and overlap
+// (programmatic dependent launch) should all ask for the same split: an SM can
+// only change its split while idle, so kernels that want different splits
+// cannot share an SM.
 template <typename Kernel>
-cudaError_t ensure_smem_limit(SmemLimit &lim, Kernel kern, int smem)
+cudaError_t ensure_smem_limit(SmemLimit &lim, Kernel kern, int smem, bool max_carveout = false)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
@@ -150,7 +155,14 @@ cudaError_t ensure_smem_limit(SmemLimit &lim, Kernel kern, int smem)
     if (lim.bytes[dev].load(std::memory_order_acquire) >= smem)
         return cudaSuccess;
     std::lock_guard<std::mutex> g(lim.mu);
-    if (lim.bytes[dev].load(std::memory_order_relaxed) < smem) {
+    const int have = lim.bytes[dev].load(std::memory_order_relaxed);
+    if (have < smem) {
+        if (have == 0 && max_carveout) {
+            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                       cudaSharedmemCarveoutMaxShared);
+            if (e != cudaSuccess)
+                return e;
+        }
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return e;

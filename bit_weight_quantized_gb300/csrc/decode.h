@@ -1,5 +1,5 @@
-// decode.h -- the staging-free decode kernel (decode.cu): 1 <= M <= 8, groups of
-// 64 or 128, K a multiple of 8 groups, at most 32 output columns per CTA.
+// decode.h -- the staged decode kernel (decode.cu): 1 <= M <= 16, groups of 64
+// or 128, K a multiple of 8 groups, weights staged in shared memory by bulk copies.
 #pragma once
 
 #include <cstdint>
@@ -7,20 +7,45 @@
 
 namespace qmm {
 
+// Launch plan of one call: grid, row split, K segments and the shared-memory
+// layout (byte offsets from the 128-byte aligned dynamic shared memory base).
+struct DecodePlan {
+    int grid;                 // CTAs: min(N, SMs)
+    int rows_base, rows_rem;  // CTA c owns rows_base + (c < rows_rem) output columns
+    int max_rows;             // rows of the largest CTA
+    int warps;                // warps per CTA (8)
+    int kseg;                 // codes per K segment: one group per warp
+    int nseg;                 // K / kseg
+    int seg_bytes;            // kseg * b / 8: one row's bytes of one segment
+    int span;                 // segments per ring slot: nseg (whole rows) or 1
+    int pitch;                // bytes between rows in a ring slot (padded)
+    int slot_bytes;           // min(32, max_rows) * pitch
+    int slots;                // ring depth: segments in flight
+    int x_pitch;              // bytes per token of one warp's activation stage
+    int off_x, off_xsum, off_sc, off_zo, off_red, off_bar;
+    int smem;                 // dynamic shared memory per CTA
+};
+
 struct DecodeParams {
     const uint16_t *x;        // fp16 [M][K], 16-byte aligned
     const uint8_t *packed;    // [N][K*b/8], 16-byte aligned
     const uint16_t *scales;   // fp16 [N][K/G]
     const uint8_t *zeros;     // uint8 [N][K/G] or nullptr (then zero_const)
     void *y;                  // fp16 or bf16 [M][N]
-    int M, N, K, group_log2, zero_const, y_bf16;
-    int rows_base, rows_rem;  // set by launch_decode: CTA c owns rows_base + (c < rows_rem) rows
+    int *status;              // device status word
+    long long row_bytes;      // K * b / 8
+    int M, N, K, group_log2, y_bf16;
+    int zero_const;           // the zero of every group when zeros == nullptr
+    DecodePlan pl;
 };
 
-// True when the shape is one the kernel takes (with a grid of min(N, num_sms) CTAs).
-bool decode_supports(int M, int N, int K, int group, int num_sms);
+// Plans a call; false if the kernel does not take the shape (the skinny kernel
+// does).  smem_pair is the per-CTA shared memory with which two CTAs share an
+// SM, smem_optin the most one CTA may use.  Host code only.
+bool decode_plan(int M, int N, int K, int group, int bits, bool stored_zeros, int num_sms,
+                 int smem_pair, int smem_optin, DecodePlan *plan);
 
 // Launches the kernel for b = bits (1..8) with programmatic dependent launch.
-cudaError_t launch_decode(DecodeParams p, int bits, int num_sms, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams &p, int bits, cudaStream_t stream);
 
 }  // namespace qmm

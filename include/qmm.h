@@ -137,6 +137,14 @@ QMM_API qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *pac
 typedef enum { QMM_GEMV_AUTO = 0, QMM_GEMV_SKINNY = 1 } qmm_gemv_kernel;
 QMM_API qmm_status qmm_set_gemv_kernel(int kernel);
 
+/* Which kernel a qmm_gemv call of this shape would run on the current device
+ * under the current qmm_set_gemv_kernel() setting, with a 16-byte aligned
+ * `packed`: QMM_GEMV_AUTO (0) for the staged decode kernel, QMM_GEMV_SKINNY (1)
+ * for the skinny kernel, or minus a status code (-QMM_ERR_SHAPE for a shape
+ * qmm_gemv rejects, -QMM_ERR_DEVICE without a usable device).  stored_zeros is
+ * nonzero when the call passes per-group zeros.  Launches nothing. */
+QMM_API int qmm_gemv_route(int M, int N, int K, int bits, int group, int stored_zeros);
+
 /* Tiled matmul for M >= 17 (the dense-contraction regime, Tilus review
  * supporting_citations [41]: tensor-core instruction layouts).  Same
  * arguments and storage as qmm_gemv, with these differences:

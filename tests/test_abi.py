@@ -28,7 +28,7 @@ def test_header_declares_the_calls():
     syms = declared_symbols()
     for name in ("qmm_pack", "qmm_unpack", "qmm_gemv", "qmm_gemm", "qmm_w4a8", "qmm_w8a8",
                  "qmm_quantize_act", "qmm_flip_sign", "qmm_gemv_float", "qmm_set_gemv_kernel",
-                 "qmm_device_status", "qmm_status_string", "qmm_abi_version"):
+                 "qmm_gemv_route", "qmm_device_status", "qmm_status_string", "qmm_abi_version"):
         assert name in syms
 
 
@@ -96,6 +96,13 @@ def test_gemm_and_w4a8_argument_errors(lib):
     assert lib.qmm_w4a8(A16, A16, B16, A16, 128, B16, None, 65, 64, 128, None) == 3
     assert lib.qmm_w4a8(None, A16, B16, A16, 128, B16, None, 1, 64, 128, None) == 1
     assert lib.qmm_w4a8(_fake(0x10004), A16, B16, A16, 128, B16, None, 1, 64, 128, None) == 4
+
+
+def test_gemv_route_rejects_bad_shapes(lib):
+    assert lib.qmm_gemv_route(17, 64, 512, 4, 128, 0) == -3     # M <= 16
+    assert lib.qmm_gemv_route(1, 64, 512, 9, 128, 0) == -3      # bits
+    assert lib.qmm_gemv_route(1, 64, 500, 4, 128, 0) == -3      # K % group
+    assert lib.qmm_gemv_route(1, 64, 512, 4, 48, 0) == -3       # group
 
 
 def test_gemv_float_argument_errors(lib):

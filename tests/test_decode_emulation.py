@@ -151,3 +151,205 @@ def test_permuted_k_order_gives_the_plain_dot_product(b):
             D[16 * i:16 * i + 16] += A @ Bm
     ref = (2.0 ** dec_exp(b) + codes.astype(np.float64)) @ x.T
     np.testing.assert_allclose(D, ref, rtol=0, atol=1e-9 * np.abs(ref).max())
+
+
+# ---- the staged kernel end to end: placement in shared memory, reads, fold ----------
+def _f16_bits_of_int(v):
+    e = v.bit_length() - 1
+    return ((e + 15) << 10) | ((v << (10 - e)) & 0x3FF)
+
+
+def _plan_pairs(b, run):
+    """The 8 fp16 pairs of a thread's normalized 16-code run (words, code 0 at
+    bit 0), through the generated plan exactly as the kernel builds them:
+    [(2^E_lo + q_lo, 2^E_hi + q_hi)] in pair order, as exact fp16 values."""
+    from tests.test_unpack_plans import PLANS, _window
+    if b == 8:
+        out = []
+        for i in range(8):
+            v = prmt(run[i >> 1], 0x64646464, 0x4342 if i & 1 else 0x4140)
+            out.append((half(v), half(v >> 16)))
+        return out
+    P = PLANS[(b, 16)]
+    wins = [_window(run, P, u) for u in range(P["kWindows"])]
+    out = []
+    for i in range(8):
+        v = (wins[P["win"][i]] & P["mask"][i]) | P["magic"][i]
+        out.append((half(v), half(v >> 16)))
+    return out
+
+
+def _slot_codes(b):
+    """code_of_slot: the run code whose activation sits in fragment slot s."""
+    from tests.test_unpack_plans import PLANS
+    if b == 8:
+        return list(range(16))
+    P = PLANS[(b, 16)]
+    out = []
+    for s in range(16):
+        i = 2 * (s >> 2) + ((s >> 1) & 1)
+        out.append(P["hi"][i] if s & 1 else P["lo"][i])
+    return out
+
+
+def _code_exps(b):
+    """exp_of_code: E of each run code (its operand is 2^E + q)."""
+    from tests.test_unpack_plans import PLANS
+    if b == 8:
+        return [10] * 16
+    P = PLANS[(b, 16)]
+    e = [None] * 16
+    for i in range(8):
+        e[P["lo"][i]] = P["elo"][i]
+        e[P["hi"][i]] = P["ehi"][i]
+    return e
+
+
+def _emulate_staged(prob, packed, plan):
+    """y of the staged decode kernel, emulated from its plan: bulk copies place each
+    row's chunk in a ring slot at the plan's pitch; each warp stages its group of
+    every segment in fragment (slot) order and forms X and C per group; every lane
+    reads its run words and activation fragments back through the kernel's
+    address formulas (asserting each read stays in its region), extracts its code
+    pairs 2^E + q with the generated plan, and the MMA order follows the pairs.
+    Products and sums are exact (fp64 over exact fp16 values); the group fold is
+    s (acc - C - z X)."""
+    b, M, N, K, G = prob.bits, prob.M, prob.N, prob.K, prob.group
+    ng = K // G
+    nw = dec_words(b)
+    NB = G // 64
+    row_bytes = K * b // 8
+    W, kseg, nseg, S = plan["warps"], plan["kseg"], plan["nseg"], plan["slots"]
+    assert W == 8 and kseg == 8 * G
+    pitch, slot_bytes, xp = plan["pitch"], plan["slot_bytes"], plan["x_pitch"]
+    slot_rows = min(32, plan["max_rows"])
+    xf = prob.x.astype(np.float64)
+    xbits = prob.x.view(np.uint16)
+    scb = prob.scales.view(np.uint16)
+    slot_code = _slot_codes(b)
+    y = np.zeros((M, N))
+    for cta in range(plan["grid"]):
+        r0 = cta * plan["rows_base"] + min(cta, plan["rows_rem"])
+        nrows = plan["rows_base"] + (1 if cta < plan["rows_rem"] else 0)
+        sm = np.zeros(plan["smem"], dtype=np.uint8)
+        # scales / zeros of the CTA's rows, transposed to [group][row]
+        sc = np.zeros(ng * nrows, dtype=np.uint16)
+        zo = np.zeros(ng * nrows) if prob.zeros is not None else None
+        for e in range(nrows * ng):
+            row, gi = divmod(e, ng)
+            sc[gi * nrows + row] = scb[r0 + row, gi]
+            if zo is not None:
+                zo[gi * nrows + row] = float(prob.zeros[r0 + row, gi])
+        assert nrows * ng * 2 <= plan["off_zo"] - plan["off_sc"]
+        # activations: warp w's group of every segment, every token, in slot order;
+        # the group sums X[w][m][j] and offsets C[w][m][j] = sum 2^E x
+        xend = plan["off_x"] + W * M * xp
+        X = np.zeros((W, M, nseg))
+        C = np.zeros((W, M, nseg))
+        pw = 2.0 ** np.array(_code_exps(b), dtype=np.float64)
+        for w in range(W):
+            for m in range(M):
+                for j in range(nseg):
+                    for bb in range(NB):
+                        for tq in range(4):
+                            dst = plan["off_x"] + w * M * xp + m * xp + ((j * NB + bb) * 64 + 16 * tq) * 2
+                            src = j * kseg + 64 * (w * NB + bb) + 16 * tq
+                            assert plan["off_x"] <= dst and dst + 32 <= xend and src + 16 <= K
+                            run = xbits[m, src:src + 16]
+                            sm[dst:dst + 32] = run[slot_code].view(np.uint8)
+                            X[w, m, j] += xf[m, src:src + 16].sum()
+                            C[w, m, j] += (pw * xf[m, src:src + 16]).sum()
+        assert plan["off_xsum"] + W * M * nseg * 4 <= plan["off_sc"]
+        nrb = -(-nrows // 32)
+        span = plan["span"]
+        chunk = span * plan["seg_bytes"]
+        for rb in range(nrb):
+            rr = 32 * rb
+            cnt = min(32, nrows - rr)
+            tot = np.zeros((W, 32, M))
+            for j in range(nseg):
+                c, jj = divmod(j, span)
+                i = rb * (nseg // span) + c
+                slot = i % S
+                base = slot * slot_bytes
+                if jj == 0:   # the chunk's bulk copies: one per row
+                    for r in range(cnt):
+                        dst = base + r * pitch
+                        assert dst + chunk <= base + slot_rows * pitch <= plan["off_x"]
+                        src = (r0 + rr + r) * row_bytes + c * chunk
+                        sm[dst:dst + chunk] = packed.reshape(-1)[src:src + chunk]
+                for w in range(W):
+                    gidx = j * W + w
+                    acc = np.zeros((32, M))
+                    for bb in range(NB):
+                        A = np.zeros((32, 16 * 4))    # [row][16 t + slot] = q of the code in that slot
+                        for g in range(8):
+                            for t in range(4):
+                                first_b = (16 * b * t) // 32 * 4
+                                o = 16 * (t & 1) if b & 1 else 0
+                                for i2 in range(2):
+                                    for h in range(2):
+                                        row = 16 * i2 + 8 * h + g
+                                        lr = min(row, cnt - 1)
+                                        a = (base + lr * pitch + jj * plan["seg_bytes"] + (64 * (w * NB + bb)) * b // 8
+                                             + first_b)
+                                        assert base <= a and a + 4 * nw <= base + lr * pitch + (jj + 1) * plan["seg_bytes"]
+                                        if b == 4:
+                                            assert a % 8 == 0
+                                        if b == 8:
+                                            assert a % 16 == 0
+                                        raw = [int(v) for v in sm[a:a + 4 * nw].view("<u4")]
+                                        run = [funnelshift_r(raw[k], raw[k + 1] if k + 1 < nw else 0, o)
+                                               if b & 1 else raw[k] for k in range(nw)]
+                                        for pi, (qlo, qhi) in enumerate(_plan_pairs(b, run)):
+                                            jp, hp = divmod(pi, 2)
+                                            A[row, 16 * t + 4 * jp + 2 * hp] = qlo
+                                            A[row, 16 * t + 4 * jp + 2 * hp + 1] = qhi
+                        Xf = np.zeros((64, M))
+                        for m in range(M):
+                            for t in range(4):
+                                a = plan["off_x"] + w * M * xp + m * xp + ((j * NB + bb) * 64 + 16 * t) * 2
+                                assert a + 32 <= xend
+                                Xf[16 * t:16 * t + 16, m] = sm[a:a + 32].view(np.float16).astype(np.float64)
+                        acc += A @ Xf
+                    for row in range(32):
+                        lr = min(row, cnt - 1)
+                        e = gidx * nrows + rr + lr
+                        s = float(np.array([sc[e]], dtype=np.uint16).view(np.float16)[0])
+                        z = zo[e] if zo is not None else float(prob.zero_const)
+                        tot[w, row] += s * (acc[row] - C[w, :, j] - z * X[w, :, j])
+            y[:, r0 + rr:r0 + rr + cnt] = tot.sum(axis=0)[:cnt].T
+    return y
+
+
+@pytest.mark.parametrize("b,M,N,K,G,zm,sms", [
+    (4, 1, 40, 1024, 128, "half", 4), (3, 3, 75, 1024, 64, "group", 2),
+    (8, 2, 37, 2048, 128, "group", 1), (1, 9, 33, 512, 64, "const8", 1),
+    (7, 2, 66, 1024, 128, "half", 2), (5, 1, 8, 2048, 64, "group", 4),
+    (6, 16, 20, 1024, 128, "half", 1), (2, 4, 19, 1024, 64, "group", 1)])
+def test_staged_kernel_emulation_matches_oracle(b, M, N, K, G, zm, sms, tmp_path):
+    import oracle
+    import synthetic
+    from tests.test_planner import SMEM_OPTIN, SMEM_PAIR, decode_plans
+    prob = synthetic.make_qmm(M, N, K, b, G, zero_mode=zm, seed=b + 10 * M)
+    # a small SM count gives several row blocks per CTA and rows past 32
+    plan = decode_plans([(M, N, K, G, b, 1 if prob.zeros is not None else 0, sms, SMEM_PAIR, SMEM_OPTIN)],
+                        tmp_path)[0]
+    assert plan is not None
+    packed, _ = oracle.pack(prob.codes, b)
+    y = _emulate_staged(prob, packed, plan)
+    ref = oracle.solve_qmm(prob)
+    np.testing.assert_allclose(y, ref, rtol=0, atol=1e-9 * max(1.0, np.abs(ref).max()))
+
+
+def test_staged_kernel_emulation_small_ring(tmp_path):
+    # a budget that leaves two slots for eight segments: the ring is reused
+    import oracle
+    import synthetic
+    from tests.test_planner import decode_plans
+    prob = synthetic.make_qmm(2, 40, 4096, 8, 128, zero_mode="half", seed=3)
+    plan = decode_plans([(2, 40, 4096, 128, 8, 0, 1, 95000, 95000)], tmp_path)[0]
+    assert plan is not None and plan["slots"] < 2 * plan["nseg"]
+    y = _emulate_staged(prob, oracle.pack(prob.codes, 8)[0], plan)
+    ref = oracle.solve_qmm(prob)
+    np.testing.assert_allclose(y, ref, rtol=0, atol=1e-9 * np.abs(ref).max())

@@ -1,7 +1,7 @@
-"""GPU parity of qmm_gemv's two kernels on the decode shapes (M <= 8, groups
-of 64 or 128, K a multiple of 8 groups, N <= 32 x the SM count), against the
-CPU oracle through the C ABI: the staging-free decode kernel (the default
-route for these shapes) and the skinny kernel (forced with
+"""GPU parity of qmm_gemv's two kernels on the shapes the staged decode kernel
+takes (1 <= M <= 16, groups of 64 or 128, K a multiple of 512), against the
+CPU oracle through the C ABI: the staged decode kernel (the default route for
+these shapes, checked with qmm_gemv_route) and the skinny kernel (forced with
 qmm_set_gemv_kernel)."""
 import numpy as np
 import pytest
@@ -33,8 +33,8 @@ def _sms():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
-def _decode_route(M, N, K, G):
-    return M <= 8 and G in (64, 128) and K % (8 * G) == 0 and N <= 32 * _sms()
+def _route(q, prob):
+    return q.qmm_gemv_route(prob.M, prob.N, prob.K, prob.bits, prob.group, prob.zeros is not None)
 
 
 def _run(q, prob, out_dtype=torch.float16):
@@ -51,32 +51,34 @@ CASES = []
 for bits in range(1, 9):
     for (M, N, K, G, zm) in [(1, 37, 512, 64, "group"), (3, 300, 1024, 128, "half"),
                              (8, 4000, 512, 64, "const8"), (5, 1, 2048, 128, "none"),
-                             (2, 153, 4096, 64, "group"), (7, 4096, 1024, 128, "group")]:
+                             (2, 153, 4096, 64, "group"), (7, 4096, 1024, 128, "group"),
+                             (9, 500, 2048, 128, "group"), (16, 333, 1536, 64, "half"),
+                             (12, 5000, 512, 64, "group")]:
         CASES.append((bits, M, N, K, G, zm))
 
 
 @pytest.mark.parametrize("bits,M,N,K,G,zm", CASES)
 def test_decode_shapes_parity(q, kernel, bits, M, N, K, G, zm):
-    assert _decode_route(M, N, K, G)
     prob = synthetic.make_qmm(M, N, K, bits, G, zero_mode=zm, seed=bits * 31 + M)
+    assert _route(q, prob) == ("decode" if kernel == "auto" else "skinny")
     assert rel_err(_run(q, prob), oracle_y(prob)) <= REL_TOL
     assert q.qmm_device_status() == 0
 
 
 @pytest.mark.parametrize("bits", [1, 4, 7, 8])
-def test_decode_most_rows_per_cta(q, kernel, bits):
-    # 32 output columns in every CTA, the most the decode kernel takes
-    N = 32 * _sms()
-    prob = synthetic.make_qmm(2, N, 512, bits, 64, zero_mode="group", seed=bits)
+@pytest.mark.parametrize("M", [2, 13])
+def test_decode_several_row_blocks_per_cta(q, kernel, bits, M):
+    # 32 x SMs + 1 columns: some CTAs own 33 rows, i.e. two row blocks
+    N = 32 * _sms() + 1
+    prob = synthetic.make_qmm(M, N, 512, bits, 64, zero_mode="group", seed=bits)
     assert rel_err(_run(q, prob), oracle_y(prob)) <= REL_TOL
 
 
 @pytest.mark.parametrize("bits", [3, 4])
-def test_one_column_past_the_decode_range(q, bits):
-    # N = 32 x SMs + 1: the skinny kernel takes the call
-    N = 32 * _sms() + 1
-    assert not _decode_route(1, N, 1024, 128)
-    prob = synthetic.make_qmm(1, N, 1024, bits, 128, zero_mode="half", seed=bits)
+def test_group_32_takes_the_skinny_kernel(q, bits):
+    # a 64-code block holds two groups of 32: the staged kernel does not take it
+    prob = synthetic.make_qmm(1, 700, 1024, bits, 32, zero_mode="half", seed=bits)
+    assert _route(q, prob) == "skinny"
     assert rel_err(_run(q, prob), oracle_y(prob)) <= REL_TOL
 
 

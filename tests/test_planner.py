@@ -121,30 +121,115 @@ def test_decode_shapes_fit_two_ctas_per_sm(plans):
 
 
 # ---- the decode kernel's shape rule (decode.cu) ------------------------------------
-def _decode_rule(M, N, K, G, sms):
-    """M <= 8, G in {64, 128}, K a positive multiple of 8 G, at most 32 columns per CTA
-    with min(N, SMs) CTAs."""
-    grid = min(N, sms)
-    return 1 <= M <= 8 and G in (64, 128) and K >= 8 * G and K % (8 * G) == 0 and -(-N // grid) <= 32
+DECODE_FIELDS = ("grid", "rows_base", "rows_rem", "max_rows", "warps", "kseg", "nseg", "seg_bytes", "span", "pitch",
+                 "slot_bytes", "slots", "x_pitch", "off_x", "off_xsum", "off_sc", "off_zo", "off_red",
+                 "off_bar", "smem")
+SMEM_PAIR, SMEM_OPTIN = 115712, 232448   # GB300: half an SM's shared memory per CTA, and the opt-in limit
 
 
-def test_decode_route_rule(tmp_path):
+def decode_plans(shapes, tmp_dir):
+    """Runs tests/decode_route_check.cu on (M, N, K, G, bits, zeros, sms, pair, optin)
+    tuples; returns None (skinny kernel) or a dict of the DecodePlan per shape."""
     nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
     if not os.path.exists(nvcc):
         pytest.skip("nvcc not available")
-    exe = str(tmp_path / "decode_route_check")
-    subprocess.run([nvcc, "-std=c++17", "-O1", "-gencode", "arch=compute_103a,code=sm_103a",
-                    "--expt-relaxed-constexpr", "-o", exe, os.path.join(HERE, "decode_route_check.cu")],
-                   check=True, capture_output=True)
-    shapes = [(M, N, K, G, sms) for M in (0, 1, 8, 9, 16) for G in (32, 64, 128)
-              for K in (256, 512, 1024, 1536, 4096, 12288)
-              for N in (1, 151, 152, 4096, 4863, 4864, 4865, 14336)
-              for sms in (152, 148)]
-    stdin = "".join(" ".join(map(str, s)) + "\n" for s in shapes)
+    exe = os.path.join(str(tmp_dir), "decode_route_check")
+    if not os.path.exists(exe):
+        subprocess.run([nvcc, "-std=c++17", "-O1", "-gencode", "arch=compute_103a,code=sm_103a",
+                        "--expt-relaxed-constexpr", "-o", exe, os.path.join(HERE, "decode_route_check.cu")],
+                       check=True, capture_output=True)
+    stdin = "".join(" ".join(map(str, sh)) + "\n" for sh in shapes)
     out = subprocess.run([exe], input=stdin, capture_output=True, text=True, check=True).stdout
-    rows = [tuple(map(int, line.split())) for line in out.splitlines()]
-    assert len(rows) == len(shapes)
-    for r in rows:
-        assert bool(r[5]) == _decode_rule(*r[:5]), r
-    # the decode sweep's shape takes the decode kernel, the skinny batch shapes do not
-    assert _decode_rule(1, 4096, 4096, 128, 152) and not _decode_rule(16, 14336, 4096, 64, 152)
+    res = []
+    for line, sh in zip(out.splitlines(), shapes):
+        v = list(map(int, line.split()))
+        assert tuple(v[:9]) == tuple(sh)
+        res.append(dict(zip(DECODE_FIELDS, v[10:])) if v[9] else None)
+    assert len(res) == len(shapes)
+    return res
+
+
+def _decode_shapes():
+    s = []
+    for sms in (152, 148, 4):
+        for b in range(1, 9):
+            for M in (1, 3, 8, 9, 16, 17):
+                for (N, K, G, z) in [(4096, 4096, 128, 0), (11008, 4096, 64, 1), (14336, 4096, 64, 1),
+                                     (37, 512, 64, 1), (300, 1024, 128, 0), (4000, 512, 64, 0),
+                                     (1, 2048, 128, 0), (4865, 1024, 128, 1), (20000, 65536, 128, 0),
+                                     (150, 1536, 128, 1), (64, 1000, 64, 0), (64, 768, 128, 0),
+                                     (64, 1024, 32, 0)]:
+                    s.append((M, N, K, G, b, z, sms, SMEM_PAIR, SMEM_OPTIN))
+    return s
+
+
+@pytest.fixture(scope="module")
+def dplans(tmp_path_factory):
+    shapes = _decode_shapes()
+    return list(zip(shapes, decode_plans(shapes, tmp_path_factory.mktemp("decode"))))
+
+
+def test_decode_route_rule(dplans):
+    # the shapes the kernel may take: 1 <= M <= 16, groups of 64 / 128, K a positive
+    # multiple of 8 groups; the rest go to the skinny kernel
+    for (M, N, K, G, b, z, sms, pair, optin), pl in dplans:
+        eligible = 1 <= M <= 16 and G in (64, 128) and K >= 8 * G and K % (8 * G) == 0
+        if not eligible:
+            assert pl is None, (M, N, K, G, b)
+    plan = {sh[:6] + (sh[6],): pl for sh, pl in dplans}
+    for b in range(1, 9):
+        # the decode sweep and the skinny batched-decode shapes take the staged kernel
+        assert plan[(1, 4096, 4096, 128, b, 0, 152)] is not None
+        for M in (3, 8, 9, 16):
+            assert plan[(M, 14336, 4096, 64, b, 1, 152)] is not None
+            assert plan[(M, 11008, 4096, 64, b, 1, 152)] is not None
+
+
+def test_decode_plan_layout(dplans):
+    resid = {1: 16, 2: 16, 3: 16, 4: 32, 5: 16, 6: 16, 7: 16, 8: 64}
+    for (M, N, K, G, b, z, sms, pair, optin), pl in dplans:
+        if pl is None:
+            continue
+        key = (M, N, K, G, b, z, sms)
+        assert pl["grid"] == min(N, sms), key
+        assert pl["grid"] * pl["rows_base"] + pl["rows_rem"] == N and pl["rows_rem"] < pl["grid"], key
+        assert pl["max_rows"] == pl["rows_base"] + (pl["rows_rem"] > 0), key
+        # 8 warps; warp w owns group w of every segment
+        assert pl["warps"] == 8, key
+        assert pl["kseg"] == 8 * G and pl["nseg"] * pl["kseg"] == K, key
+        assert pl["seg_bytes"] == pl["kseg"] * b // 8 and pl["seg_bytes"] % 16 == 0, key
+        # a slot holds whole rows (every row block at once) or one segment
+        assert pl["span"] in (1, pl["nseg"]), key
+        chunk = pl["span"] * pl["seg_bytes"]
+        assert pl["pitch"] >= chunk and pl["pitch"] % 16 == 0, key
+        assert pl["pitch"] % 128 == resid[b], key
+        slot_rows = min(32, pl["max_rows"])
+        assert pl["slot_bytes"] == slot_rows * pl["pitch"], key
+        total = _ceil(pl["max_rows"], 32) * (pl["nseg"] // pl["span"])
+        assert 1 <= pl["slots"] <= min(total, 16), key
+        assert pl["slots"] == total or pl["slots"] >= 2, key
+        if pl["span"] == pl["nseg"] and pl["nseg"] > 1:
+            assert pl["slots"] == total, key
+        # regions in order, aligned, without overlap, inside the budget
+        assert pl["slots"] * pl["slot_bytes"] <= pl["off_x"] and pl["off_x"] % 16 == 0, key
+        assert pl["x_pitch"] == K // pl["warps"] * 2 + 16, key
+        assert pl["off_x"] + pl["warps"] * M * pl["x_pitch"] <= pl["off_xsum"], key
+        assert pl["off_xsum"] + pl["warps"] * M * pl["nseg"] * 4 <= pl["off_sc"], key
+        ng = K // G
+        assert pl["off_sc"] + pl["max_rows"] * ng * 2 <= pl["off_zo"], key
+        assert pl["off_zo"] + (pl["max_rows"] * ng * 2 if z else 0) <= pl["off_red"], key
+        assert pl["off_red"] + pl["warps"] * 32 * M * 4 <= pl["off_bar"] and pl["off_bar"] % 8 == 0, key
+        assert pl["off_bar"] + 2 * pl["slots"] * 8 + 4 <= pl["smem"] <= optin, key
+
+
+def test_decode_sweep_keeps_two_ctas_per_sm_and_preloads(dplans):
+    # the decode sweep fits two CTAs per SM (one call computing while the next
+    # one's weights stream in); up to b = 7 a CTA's whole weight share is in
+    # flight before its dependency wait, at b = 8 three quarters
+    for (M, N, K, G, b, z, sms, pair, optin), pl in dplans:
+        if (M, N, K, G, z, sms) == (1, 4096, 4096, 128, 0, 152):
+            assert pl["smem"] <= SMEM_PAIR, b
+            if b <= 7:   # one bulk copy per row, the whole of K
+                assert pl["span"] == pl["nseg"] and pl["slots"] == 1, b
+            else:
+                assert pl["span"] == 1 and pl["slots"] * 4 >= pl["nseg"] * 3, b
