@@ -173,15 +173,14 @@ __device__ __forceinline__ void block_mma(const uint8_t *sb, int pitch, const in
                               a[i][1][2 * j + 1], xw[tt][2 * j], xw[tt][2 * j + 1]);
 }
 
-// Stages one 16-code run of activations in fragment (slot) order: slot s of the
-// run holds x of the run's code code_of_slot(s).  Returns the run's sums
-// X = sum x and C = sum 2^E x (E of each code's position in the plan), in fp32.
+// Stores one 16-code run of activations (in[8] = its 16 fp16 values in code
+// order) in fragment (slot) order: slot s of the run holds x of the run's code
+// code_of_slot(s).  Returns the run's sums X = sum x and C = sum 2^E x (E of
+// each code's position in the plan), in fp32.
 template <int B>
-__device__ __forceinline__ float2 stage_run(uint8_t *dst, const uint16_t *src)
+__device__ __forceinline__ float2 stage_run(uint8_t *dst, const uint4 (&raw)[2])
 {
-    const uint4 lo = *reinterpret_cast<const uint4 *>(src);
-    const uint4 hi = *reinterpret_cast<const uint4 *>(src + 8);
-    const uint32_t in[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    const uint32_t in[8] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w};
     uint32_t out[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
@@ -198,6 +197,56 @@ __device__ __forceinline__ float2 stage_run(uint8_t *dst, const uint16_t *src)
         C = fmaf(static_cast<float>(1 << exp_of_code<B, 16>(c)), v, C);
     }
     return make_float2(X, C);
+}
+
+// The activation staging of more than one round (several tokens or long K),
+// kept out of line so that the one-round path of the decode shapes stays compact.
+template <int B, int NB>
+__device__ __noinline__ void stage_rounds(const DecodeParams &p, uint8_t *xw, float2 *xs, int warp, int lane,
+                                          int rounds)
+{
+    constexpr int kBatch = 4;
+    constexpr int jstep = 8 / NB;                       // segments per round
+    const DecodePlan &pl = p.pl;
+    const int tq = lane & 3, bb = (lane >> 2) & (NB - 1), jl = lane >> (NB == 2 ? 3 : 2);
+        int mr = 0, jr = 0;                             // token and first segment of the next round
+        for (int r0 = 0; r0 < rounds; r0 += kBatch) {
+            uint4 raw[kBatch][2];
+            int mq[kBatch], jq[kBatch];
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                mq[q] = mr;
+                jq[q] = r0 + q < rounds ? jr + jl : pl.nseg;   // nseg marks an idle lane
+                if (jq[q] < pl.nseg) {
+                    const uint16_t *src = p.x + static_cast<long long>(mq[q]) * p.K + jq[q] * pl.kseg +
+                                          64 * (warp * NB + bb) + 16 * tq;
+                    raw[q][0] = *reinterpret_cast<const uint4 *>(src);
+                    raw[q][1] = *reinterpret_cast<const uint4 *>(src + 8);
+                } else {
+                    raw[q][0] = raw[q][1] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                jr += jstep;
+                if (jr >= pl.nseg) {
+                    jr = 0;
+                    ++mr;
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                if (r0 + q >= rounds)
+                    break;
+                float2 v = make_float2(0.f, 0.f);
+                if (jq[q] < pl.nseg)
+                    v = stage_run<B>(xw + mq[q] * pl.x_pitch + ((jq[q] * NB + bb) * 64 + 16 * tq) * 2, raw[q]);
+#pragma unroll
+                for (int off = 1; off < 4 * NB; off <<= 1) {
+                    v.x += __shfl_xor_sync(0xffffffffu, v.x, off);
+                    v.y += __shfl_xor_sync(0xffffffffu, v.y, off);
+                }
+                if (jq[q] < pl.nseg && (lane & (4 * NB - 1)) == 0)
+                    xs[mq[q] * pl.nseg + jq[q]] = v;   // (X, C) of the token, this warp's group of segment jq
+            }
+        }
 }
 
 // NB = G / 64 blocks per group; warp w owns group w of every 8-group segment.
@@ -271,26 +320,32 @@ decode_kernel(const DecodeParams p)
     uint8_t *xw = smem + pl.off_x + warp * (p.M * pl.x_pitch);
     float2 *xs = reinterpret_cast<float2 *>(xsum) + warp * p.M * pl.nseg;
     {
-        const int nrun = p.M * pl.nseg * NB * 4;
-        for (int u0 = 0; u0 < nrun; u0 += 32) {
-            const int u = u0 + lane;
+        // A round is 32 runs, one per lane: lane l takes run tq = l & 3 of block
+        // bb = (l >> 2) % NB of segment jb + (l >> 2) / NB of one token; the
+        // 4 NB lanes of one (token, segment) meet in the shuffle sum.  Rounds go
+        // token by token, segment block by segment block, and kBatch rounds'
+        // loads are issued before any is used.
+        constexpr int jstep = 8 / NB;                   // segments per round
+        const int tq = lane & 3, bb = (lane >> 2) & (NB - 1), jl = lane >> (NB == 2 ? 3 : 2);
+        const int rounds = p.M * ((pl.nseg + jstep - 1) / jstep);
+        if (rounds == 1) {   // one round (a single token and at most jstep segments)
             float2 v = make_float2(0.f, 0.f);
-            int m = 0, j = 0;
-            if (u < nrun) {
-                const int tq = u & 3, bb = (u >> 2) % NB, mj = u / (4 * NB);
-                m = mj / pl.nseg;
-                j = mj - m * pl.nseg;
-                v = stage_run<B>(xw + m * pl.x_pitch + ((j * NB + bb) * 64 + 16 * tq) * 2,
-                                 p.x + static_cast<long long>(m) * p.K + j * pl.kseg + 64 * (warp * NB + bb) + 16 * tq);
+            if (jl < pl.nseg) {
+                const uint16_t *src = p.x + jl * pl.kseg + 64 * (warp * NB + bb) + 16 * tq;
+                const uint4 raw[2] = {*reinterpret_cast<const uint4 *>(src),
+                                      *reinterpret_cast<const uint4 *>(src + 8)};
+                v = stage_run<B>(xw + ((jl * NB + bb) * 64 + 16 * tq) * 2, raw);
             }
 #pragma unroll
             for (int off = 1; off < 4 * NB; off <<= 1) {
                 v.x += __shfl_xor_sync(0xffffffffu, v.x, off);
                 v.y += __shfl_xor_sync(0xffffffffu, v.y, off);
             }
-            if (u < nrun && (lane & (4 * NB - 1)) == 0)
-                xs[m * pl.nseg + j] = v;   // (X, C) of token m, this warp's group of segment j
+            if (jl < pl.nseg && (lane & (4 * NB - 1)) == 0)
+                xs[jl] = v;
         }
+        if (rounds > 1)
+            stage_rounds<B, NB>(p, xw, xs, warp, lane, rounds);
         __syncwarp();
     }
 

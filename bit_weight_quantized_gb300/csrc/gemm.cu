@@ -602,7 +602,7 @@ qmm_status launch_gemm(const CUtensorMap &tmx, const CUtensorMap &tmw, GemmParam
         return QMM_ERR_UNSUPPORTED;
     p.passes = (p.mtiles + MT - 1) / MT;
     static SmemLimit limit;
-    if (ensure_smem_limit(limit, gemm_kernel<MT, S>, smem) != cudaSuccess)
+    if (ensure_smem_limit(limit, gemm_kernel<MT, S>, smem, true) != cudaSuccess)
         return QMM_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

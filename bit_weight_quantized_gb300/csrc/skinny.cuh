@@ -722,7 +722,7 @@ cudaError_t launch_skinny(const GemvParams &p, int grid, int smem, cudaStream_t 
 {
     auto kern = skinny_kernel<B, NT, R, MODE>;
     static SmemLimit limit;
-    if (const cudaError_t e = ensure_smem_limit(limit, kern, smem); e != cudaSuccess)
+    if (const cudaError_t e = ensure_smem_limit(limit, kern, smem, true); e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
