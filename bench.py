@@ -48,7 +48,7 @@ WORKLOAD = ("decode GEMV width sweep: M=1, K=N=4096, bits 1..8, group 128, "
             "z=2^(b-1), fp16 activations/outputs, fp32 accumulation")
 BITS = list(range(1, 9))
 PROFILE = os.path.join(ROOT, "profiles", "qmm_gemv_decode_sweep.txt")
-KERNEL_SOURCES = ["decode.cu", "decode.h", "common.cuh"]
+KERNEL_SOURCES = ["decode.cu", "decode.h", "common.cuh", "extract.cuh", "unpack_plans.h"]
 
 
 def kernel_source_digest() -> str:
