@@ -356,6 +356,19 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf, gemv_kernel="auto",
         out[f"tiled_M{M}"] = {"us": round(ms * 1e3, 1), "TFLOPs": round(tf, 1),
                               "frac_bf16": round(tf / peak_tf, 4)}
     del wsets
+    # the tiled path at the other widths: M = 512, K = 8192, N = 28672, group 128,
+    # z = 2^(b-1), bf16
+    M = 512
+    x = torch.randn(M, K, device=dev, generator=gen).bfloat16()
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    for b in (1, 2, 3, 5, 6, 7, 8):
+        wsets = [(q.qmm_pack(codes(N, K, b), b), scales(N, K // 128)) for _ in range(ncopies(N * K * b // 8))]
+        ms = time_graph(torch, stream, [lambda w=w_, b=b: q.qmm_gemm(x, w[0], b, 128, w[1], None, 1 << (b - 1), out=y)
+                                        for w_ in wsets], reps=3)
+        tf = 2.0 * M * N * K / ms / 1e9
+        out[f"tiled_M{M}_b{b}"] = {"us": round(ms * 1e3, 1), "TFLOPs": round(tf, 1),
+                                   "frac_bf16": round(tf / peak_tf, 4)}
+        del wsets
     # W4A8: K=N=4096, group 128
     N = K = 4096
     wsets = [(q.qmm_pack(codes(N, K, 4), 4), scales(N, K // 128)) for _ in range(ncopies(N * K // 2))]

@@ -1,0 +1,5 @@
+// gemm_w1.cu -- the tiled kernel for 1-bit weights (one width per file so
+// that the widths compile in parallel).
+#include "gemm.cuh"
+
+QMM_GEMM_WIDTH(1)

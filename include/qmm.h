@@ -151,9 +151,11 @@ QMM_API int qmm_gemv_route(int M, int N, int K, int bits, int group, int stored_
  *   - x and y may be QMM_BF16 or QMM_F16 (x_dtype == y_dtype);
  *   - x, y and packed must be 16-byte aligned and K * bits / 8 (the packed
  *     row pitch) a multiple of 16 bytes (else QMM_ERR_ALIGN);
- *   - bits must be 4 (else QMM_ERR_UNSUPPORTED).
- * Weights are dequantized to bf16/fp16 (q - z) * s tiles in shared memory
- * (one rounding of the exact product; q - z itself is exact for every zero
+ *   - any width 1..8 (the Tilus review's one matmul for every width).
+ * Packed weights arrive by TMA in stages (128-byte swizzled boxes per row at
+ * widths 1, 2, 4 and 8; two 64-code K steps per stage at the other widths),
+ * are dequantized to bf16/fp16 (q - z) * s tiles in shared memory (one
+ * rounding of the exact product; q - z itself is exact for every zero
  * 0..255) and multiplied with tcgen05 MMAs accumulating in fp32 in tensor
  * memory.  With fp16 the dequantized weight must be finite in fp16:
  * |q - z| * s < 65504. */

@@ -72,11 +72,45 @@ def test_gemm_deterministic(q):
     np.testing.assert_array_equal(a, b)
 
 
-def test_gemm_rejects_other_widths(q):
-    prob = synthetic.make_qmm(32, 192, 256, 3, 128, zero_mode="const8", seed=1)
-    x, packed, scales, _ = to_dev_problem(prob)
-    with pytest.raises(q.QmmError):
-        q.qmm_gemm(x, packed, 3, 128, scales, None, 8)
+WIDTH_CASES = []
+for _b in range(1, 9):
+    for (M, N, K, G, zm, dt) in [(17, 192, 256, 128, "half", "f16"), (130, 300, 1024, 64, "group", "bf16"),
+                                 (200, 193, 2048, 128, "none", "bf16"), (129, 384, 512, 32, "half", "f16"),
+                                 (300, 200, 1536, 128, "group", "f16"), (256, 250, 640, 32, "half", "bf16")]:
+        WIDTH_CASES.append((_b, M, N, K, G, zm, dt))
+
+
+@pytest.mark.parametrize("bits,M,N,K,G,zm,dt", WIDTH_CASES)
+def test_gemm_every_width_parity(q, bits, M, N, K, G, zm, dt):
+    """The tiled path at widths 1..8 (Tilus review: one matmul for any width);
+    K * b / 8 must be a multiple of 16 bytes."""
+    if (K * bits // 8) % 16:
+        pytest.skip("packed row pitch not a multiple of 16 bytes")
+    prob = synthetic.make_qmm(M, N, K, bits, G, zero_mode=zm, x_dtype=dt, y_dtype=dt,
+                              seed=bits * 101 + M)
+    check(prob, run_gemm(q, prob), oracle_y(prob))
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("bits", [1, 2, 3, 5, 6, 7, 8])
+def test_gemm_every_width_extreme_zeros(q, bits, dt):
+    # codes at both ends and zeros up to 255 (bf16 cannot hold 2^E + z for large z)
+    prob = synthetic.make_qmm(144, 256, 1024, bits, 64, zero_mode="group", x_dtype=dt, y_dtype=dt,
+                              seed=bits)
+    st = SplitMix64(bits + 50)
+    prob.zeros = st.uniform_bits(prob.zeros.size, 8).reshape(prob.zeros.shape)
+    prob.codes[:, ::7] = (1 << bits) - 1
+    prob.codes[:, 3::7] = 0
+    check(prob, run_gemm(q, prob), oracle_y(prob))
+
+
+@pytest.mark.parametrize("bits", range(1, 9))
+def test_gemm_every_width_config4_k_sampled(q, bits):
+    """Config-4-like: K = 8192, M = 128, bf16, group 128, z = 2^(b-1); N = 1536
+    (8 column tiles), every output checked."""
+    prob = synthetic.make_qmm(128, 1536, 8192, bits, 128, zero_mode="half", x_dtype="bf16",
+                              y_dtype="bf16", seed=bits + 900)
+    check(prob, run_gemm(q, prob), oracle_y(prob))
 
 
 @pytest.mark.parametrize("M", [128, 512, 2048])
