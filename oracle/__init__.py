@@ -90,6 +90,12 @@ def _load():
             lib.oracle_interleave4.restype = None
             lib.oracle_deinterleave4.argtypes = [P, P, L, L]
             lib.oracle_deinterleave4.restype = None
+            lib.oracle_tile16_bytes.argtypes = [L, L, I]
+            lib.oracle_tile16_bytes.restype = L
+            lib.oracle_tile16.argtypes = [P, P, L, L, I]
+            lib.oracle_tile16.restype = None
+            lib.oracle_untile16.argtypes = [P, P, L, L, I]
+            lib.oracle_untile16.restype = None
             _lib = lib
     return _lib
 
@@ -294,6 +300,32 @@ def deinterleave4(packed: np.ndarray, K: int) -> np.ndarray:
         raise ValueError("packed row length must be K/2, K a multiple of 8")
     out = np.empty((N, K), dtype=np.uint8)
     _load().oracle_deinterleave4(_ptr(packed), _ptr(out), N, K)
+    return out
+
+
+def tile16_bytes(N: int, K: int, bits: int) -> int:
+    return int(_load().oracle_tile16_bytes(N, K, bits))
+
+
+def tile16(codes: np.ndarray, bits: int) -> np.ndarray:
+    """uint8 codes [N][K] (K % 64 == 0) -> the fragment-ordered tile16 stream
+    (uint8, ceil(N/16)*16*K*bits/8 bytes)."""
+    codes = _c(codes, np.uint8)
+    N, K = codes.shape
+    if K % 64:
+        raise ValueError("K must be a multiple of 64")
+    out = np.empty(tile16_bytes(N, K, bits), dtype=np.uint8)
+    _load().oracle_tile16(_ptr(codes), _ptr(out), N, K, bits)
+    return out
+
+
+def untile16(stream: np.ndarray, N: int, K: int, bits: int) -> np.ndarray:
+    """Inverse of tile16 -> codes uint8 [N][K]."""
+    stream = _c(stream, np.uint8)
+    if stream.size != tile16_bytes(N, K, bits):
+        raise ValueError("stream length must be tile16_bytes(N, K, bits)")
+    out = np.empty((N, K), dtype=np.uint8)
+    _load().oracle_untile16(_ptr(stream), _ptr(out), N, K, bits)
     return out
 
 

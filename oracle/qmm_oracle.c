@@ -54,6 +54,19 @@
  *     the bytes of (W & 0xF0F0F0F0) >> 4 are codes 4..7: one shift and two
  *     masks give four byte-aligned values each (Fig. 8(b); the page prints
  *     the first mask garbled as 0xF0F0F0F0 for both halves).
+ *  9. Fragment-ordered ("tile16") layout, a reading of the pre-permuted,
+ *     MMA-fragment-ordered bitstreams the pages point to (BitLLM sec. 4.3:
+ *     weights are re-laid out offline so that each thread's loads are
+ *     contiguous and need no reordering; the pages fix no order for a
+ *     tensor-core fragment).  Rows are taken in tiles of 16 (the last tile
+ *     padded with zero codes), K in blocks of 64 codes.  Unit (T, kb) holds
+ *     rows 16T..16T+15 of codes 64kb..64kb+63 in 128*b bytes at byte
+ *     (T*(K/64) + kb)*128*b.  Inside it, run r = (h*8 + g)*4 + t (h = 0..1,
+ *     g = 0..7, t = 0..3) is codes 16t..16t+15 of the block for row
+ *     16T + 8h + g, at bytes [2*b*r, 2*b*r + 2*b), code c of the run at bits
+ *     [c*b, c*b + b) (LSB first).  Runs are the 16-code slices one
+ *     tensor-core thread reads per row: thread (g, t) of a warp reads runs
+ *     (0, g, t) and (1, g, t) of two 8-row halves.
  *
  * Every function follows the definition directly: per-bit loops, no word
  * tricks, no blocking.
@@ -374,4 +387,49 @@ void oracle_deinterleave4(const uint8_t *in, uint8_t *codes, long N, long K)
             codes[n * K + k] = (uint8_t)((row[slot / 2] >> (4 * (slot % 2))) & 15u);
         }
     }
+}
+
+/* ---- 9. fragment-ordered (tile16) layout ---------------------------------- */
+
+/* Bit position, in the tile16 stream, of bit j of code k of row n. */
+static long tile16_bit(long n, long k, int j, long K, int bits)
+{
+    const long T = n / 16, kb = k / 64;
+    const long h = (n % 16) / 8, g = n % 8, t = (k % 64) / 16, c = k % 16;
+    const long unit = T * (K / 64) + kb;
+    const long run = (h * 8 + g) * 4 + t;
+    return unit * 128L * bits * 8 + run * 16L * bits + c * bits + j;
+}
+
+/* Bytes of the tile16 stream of N rows: ceil(N/16) tiles of 16 rows. */
+long oracle_tile16_bytes(long N, long K, int bits)
+{
+    return (N + 15) / 16 * 16 * K * bits / 8;
+}
+
+/* codes [N][K] (K % 64 == 0) -> tile16 stream; padding rows hold code 0. */
+void oracle_tile16(const uint8_t *codes, uint8_t *out, long N, long K, int bits)
+{
+    memset(out, 0, (size_t)oracle_tile16_bytes(N, K, bits));
+    for (long n = 0; n < N; ++n)
+        for (long k = 0; k < K; ++k)
+            for (int j = 0; j < bits; ++j)
+                if ((codes[n * K + k] >> j) & 1u) {
+                    const long i = tile16_bit(n, k, j, K, bits);
+                    out[i / 8] |= (uint8_t)(1u << (i % 8));
+                }
+}
+
+/* tile16 stream -> codes [N][K]. */
+void oracle_untile16(const uint8_t *in, uint8_t *codes, long N, long K, int bits)
+{
+    for (long n = 0; n < N; ++n)
+        for (long k = 0; k < K; ++k) {
+            unsigned q = 0;
+            for (int j = 0; j < bits; ++j) {
+                const long i = tile16_bit(n, k, j, K, bits);
+                q |= (unsigned)((in[i / 8] >> (i % 8)) & 1u) << j;
+            }
+            codes[n * K + k] = (uint8_t)q;
+        }
 }

@@ -485,3 +485,46 @@ def test_interleave4_is_the_canonical_pack_of_permuted_codes_and_inverts():
     np.testing.assert_array_equal(oracle.deinterleave4(inter, 136), codes)
     with pytest.raises(ValueError):
         oracle.interleave4(codes[:, :12])
+
+
+# ---- fragment-ordered (tile16) layout ---------------------------------------------------
+@pytest.mark.parametrize("case", list(_golden_lines("tile16_runs.txt")))
+def test_tile16_worked_runs(case):
+    run, hexbytes = (part.split() for part in case)
+    n = np.arange(16)[:, None]
+    k = np.arange(64)[None, :]
+    codes = ((n + k) % 16).astype(np.uint8)
+    out = oracle.tile16(codes, 4)
+    r = int(run[0])
+    assert out[8 * r:8 * r + 8].tolist() == [int(h, 16) for h in hexbytes]
+
+
+def _tile16_by_chunks(codes, bits):
+    """The tile16 stream built another way: the canonical stream cut into the
+    2b-byte slices of 16 codes (byte-aligned: code 16t of a block starts at byte
+    2bt), gathered run by run with numpy indexing."""
+    N, K = codes.shape
+    Np = -(-N // 16) * 16
+    padded = np.zeros((Np, K), dtype=np.uint8)
+    padded[:N] = codes
+    canon, _ = oracle.pack(padded, bits)                          # [Np][K*b/8]
+    runs = canon.reshape(Np // 16, 2, 8, K // 64, 4, 2 * bits)    # [T][h][g][kb][t][2b]
+    return runs.transpose(0, 3, 1, 2, 4, 5).reshape(-1)           # [T][kb][h][g][t][2b]
+
+
+@pytest.mark.parametrize("bits", range(1, 9))
+@pytest.mark.parametrize("N,K", [(16, 64), (37, 128), (5, 256), (48, 192)])
+def test_tile16_is_a_permutation_of_canonical_runs(bits, N, K):
+    st = SplitMix64(3 * bits + N + K)
+    codes = st.uniform_bits(N * K, bits).reshape(N, K)
+    out = oracle.tile16(codes, bits)
+    assert out.size == -(-N // 16) * 16 * K * bits // 8
+    np.testing.assert_array_equal(out, _tile16_by_chunks(codes, bits))
+
+
+@pytest.mark.parametrize("bits", range(1, 9))
+def test_tile16_round_trip(bits):
+    st = SplitMix64(bits + 700)
+    N, K = 29, 320
+    codes = st.uniform_bits(N * K, bits).reshape(N, K)
+    np.testing.assert_array_equal(oracle.untile16(oracle.tile16(codes, bits), N, K, bits), codes)
