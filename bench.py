@@ -48,7 +48,7 @@ WORKLOAD = ("decode GEMV width sweep: M=1, K=N=4096, bits 1..8, group 128, "
             "z=2^(b-1), fp16 activations/outputs, fp32 accumulation")
 BITS = list(range(1, 9))
 PROFILE = os.path.join(ROOT, "profiles", "qmm_gemv_decode_sweep.txt")
-KERNEL_SOURCES = ["decode.cu", "decode.h", "common.cuh", "extract.cuh", "unpack_plans.h"]
+KERNEL_SOURCES = ["decode.cu", "decode.cuh", "decode.h", "common.cuh", "extract.cuh", "unpack_plans.h"]
 
 
 def kernel_source_digest() -> str:
@@ -324,6 +324,12 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf, gemv_kernel="auto",
     nbytes = N * K * b // 8 + N * (K // G) * 3 + M * K * 2 + M * N * 2
     out["skinny_M16_N14336_b6_g64"] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
                                        "frac_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4)}
+    # the same call on weights repacked to the fragment-ordered layout
+    sets = [(q.qmm_repack(s[0], K, b, "tile16"), s[1], s[2]) for s in sets]
+    ms = time_graph(torch, stream, [lambda s=s_: q.qmm_gemv_tile16(x, s[0], N, b, G, s[1], s[2], out=y)
+                                    for s_ in sets])
+    out["tile16_M16_N14336_b6_g64"] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
+                                       "frac_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4)}
     del sets
     # the decode kernel beside the skinny kernel (forced) on the decode shape
     # K = N = 4096, b = 4, group 128, M = 1 and 8
@@ -343,6 +349,12 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf, gemv_kernel="auto",
             name = "decode" if kern == "auto" else "skinny_forced"
             out[f"{name}_M{M}_N4096_b4_g128"] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
                                                  "frac_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4)}
+        tiled = [q.qmm_repack(s[0], K, b, "tile16") for s in sets]
+        ms = time_graph(torch, stream, [lambda t=t_, s=s_: q.qmm_gemv_tile16(x, t, N, b, G, s[1], None, 8, out=y)
+                                        for t_, s_ in zip(tiled, sets)])
+        del tiled
+        out[f"tile16_M{M}_N4096_b4_g128"] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
+                                             "frac_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4)}
     del sets
     # tiled: K=8192, N=28672, int4 group 128, z=8, bf16
     N, K = 28672, 8192

@@ -45,6 +45,9 @@ SIGNATURES = {
     "qmm_quantize_act": ([_P, _P, _P, _I, _I, _P], _I),
     "qmm_set_gemv_kernel": ([_I], _I),
     "qmm_gemv_route": ([_I, _I, _I, _I, _I, _I], _I),
+    "qmm_repack_bytes": ([_I, _I, _I, _I], _SZ),
+    "qmm_repack": ([_P, _P, _I, _I, _I, _I, _P], _I),
+    "qmm_gemv_tile16": ([_P, _I, _P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P], _I),
     "qmm_device_status": ([_P], _I),
     "qmm_watchdog_selftest": ([_P], _I),
     "qmm_status_string": ([_I], ctypes.c_char_p),
@@ -171,6 +174,56 @@ def qmm_gemv(x, packed, bits, group, scales, zeros=None, zero_const=0, out=None,
              out_dtype=None) -> torch.Tensor:
     """y[M][N] = x . W^T for 1 <= M <= 16 (the decode or the skinny kernel)."""
     return _qmm("qmm_gemv", x, packed, bits, group, scales, zeros, zero_const, out, out_dtype)
+
+
+LAYOUTS = {"tile16": 1, "interleave4": 2}
+
+
+def qmm_repack_bytes(N: int, K: int, bits: int, layout: str) -> int:
+    """Bytes of the `layout` form ("tile16" or "interleave4") of an N x K
+    bits-bit weight matrix (0 if the layout does not take these sizes)."""
+    return int(load().qmm_repack_bytes(N, K, bits, LAYOUTS[layout]))
+
+
+def qmm_repack(packed: torch.Tensor, K: int, bits: int, layout: str, out: Optional[torch.Tensor] = None):
+    """Canonical packed bitstream [N][K*bits/8] -> a flat uint8 tensor in `layout`."""
+    _dev(packed, "packed", torch.uint8)
+    N = packed.shape[0]
+    if packed.shape[1] * 8 != K * bits:
+        raise ValueError("packed must be [N][K*bits/8]")
+    nbytes = qmm_repack_bytes(N, K, bits, layout)
+    if nbytes == 0 and N * K:
+        raise QmmError(3, "qmm_repack")
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=packed.device)
+    _dev(out, "out", torch.uint8, (nbytes,))
+    _check(load().qmm_repack(packed.data_ptr(), out.data_ptr(), N, K, bits, LAYOUTS[layout],
+                             _stream(packed.get_device())), "qmm_repack")
+    return out
+
+
+def qmm_gemv_tile16(x, tiled, N, bits, group, scales, zeros=None, zero_const=0, out=None,
+                    out_dtype=None) -> torch.Tensor:
+    """qmm_gemv on weights in the tile16 layout (`tiled`: the flat output of
+    qmm_repack(..., "tile16") for N output columns)."""
+    _dev(x, "x")
+    M, K = x.shape
+    _dev(tiled, "tiled", torch.uint8, (qmm_repack_bytes(N, K, bits, "tile16"),))
+    _dev(scales, "scales", torch.float16, (N, K // group))
+    if zeros is not None:
+        _dev(zeros, "zeros", torch.uint8, (N, K // group))
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else x.dtype
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    _dev(out, "out", out_dtype, (M, N))
+    fn = _FN.get("qmm_gemv_tile16") or getattr(load(), "qmm_gemv_tile16")
+    st = fn(x.data_ptr(), _DT[x.dtype], tiled.data_ptr(), bits, group, scales.data_ptr(),
+            None if zeros is None else zeros.data_ptr(), int(zero_const), out.data_ptr(),
+            _DT[out_dtype], M, N, K, _stream(x.get_device()))
+    if st:
+        raise QmmError(st, "qmm_gemv_tile16")
+    return out
 
 
 GEMV_KERNELS = {"auto": 0, "skinny": 1}

@@ -296,7 +296,8 @@ qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int
         return from_cuda(cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * 2, stream));
     DecodePlan plan;
     if (g_gemv_kernel.load(std::memory_order_relaxed) == QMM_GEMV_AUTO && aligned(packed, 16) &&
-        decode_plan(M, N, K, group, bits, zeros != nullptr, f->num_sms, f->smem_pair, f->smem_optin, &plan)) {
+        decode_plan(M, N, K, group, bits, zeros != nullptr, false, f->num_sms, f->smem_pair, f->smem_optin,
+                    &plan)) {
         DecodeParams d;
         std::memset(&d, 0, sizeof(d));
         d.x = static_cast<const uint16_t *>(x);
@@ -313,7 +314,7 @@ qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int
         d.y_bf16 = y_dtype == QMM_BF16;
         d.zero_const = zeros ? 0 : zero_const;
         d.pl = plan;
-        return from_cuda(launch_decode(d, bits, stream));
+        return from_cuda(launch_decode(d, bits, false, stream));
     }
 
     GemvParams p;
@@ -362,9 +363,81 @@ int qmm_gemv_route(int M, int N, int K, int bits, int group, int stored_zeros)
     if (g_gemv_kernel.load(std::memory_order_relaxed) != QMM_GEMV_AUTO)
         return QMM_GEMV_SKINNY;
     DecodePlan plan;
-    return decode_plan(M, N, K, group, bits, stored_zeros != 0, f->num_sms, f->smem_pair, f->smem_optin, &plan)
+    return decode_plan(M, N, K, group, bits, stored_zeros != 0, false, f->num_sms, f->smem_pair, f->smem_optin,
+                       &plan)
                ? QMM_GEMV_AUTO
                : QMM_GEMV_SKINNY;
+}
+
+size_t qmm_repack_bytes(int N, int K, int bits, int layout)
+{
+    if (N < 0 || K < 0 || bits < 1 || bits > 8)
+        return 0;
+    if (layout == QMM_LAYOUT_TILE16)
+        return K % 64 ? 0 : static_cast<size_t>((N + 15) / 16) * 16 * K * bits / 8;
+    if (layout == QMM_LAYOUT_INTERLEAVE4)
+        return bits != 4 || K % 8 ? 0 : static_cast<size_t>(N) * K / 2;
+    return 0;
+}
+
+qmm_status qmm_repack(const uint8_t *packed, uint8_t *out, int N, int K, int bits, int layout, cudaStream_t stream)
+{
+    if (bits < 1 || bits > 8)
+        return QMM_ERR_BITS;
+    if (N < 0 || K < 0 || (layout != QMM_LAYOUT_TILE16 && layout != QMM_LAYOUT_INTERLEAVE4))
+        return QMM_ERR_SHAPE;
+    if ((layout == QMM_LAYOUT_TILE16 && K % 64) || (layout == QMM_LAYOUT_INTERLEAVE4 && (bits != 4 || K % 8)))
+        return QMM_ERR_SHAPE;
+    if (N == 0 || K == 0)
+        return QMM_OK;
+    if (!packed || !out)
+        return QMM_ERR_NULL;
+    const DeviceFacts *f = device_facts();
+    if (!f || f->usable != QMM_OK)
+        return QMM_ERR_DEVICE;
+    return from_cuda(launch_repack(packed, out, N, K, bits, layout, stream, f->num_sms));
+}
+
+qmm_status qmm_gemv_tile16(const void *x, qmm_dtype x_dtype, const uint8_t *tiled, int bits, int group,
+                           const void *scales, const uint8_t *zeros, int zero_const, void *y, qmm_dtype y_dtype,
+                           int M, int N, int K, cudaStream_t stream)
+{
+    qmm_status st = check_qmm_args(x, tiled, bits, group, scales, zero_const, zeros, y, M, N, K);
+    if (st != QMM_OK)
+        return st;
+    if (M > 16)
+        return QMM_ERR_SHAPE;
+    if (x_dtype != QMM_F16 || (y_dtype != QMM_F16 && y_dtype != QMM_BF16))
+        return QMM_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0)
+        return QMM_OK;
+    if (K > 0 && !aligned(tiled, 16))
+        return QMM_ERR_ALIGN;
+    const DeviceFacts *f = device_facts();
+    if (!f || f->usable != QMM_OK)
+        return QMM_ERR_DEVICE;
+    if (K == 0)
+        return from_cuda(cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * 2, stream));
+    DecodePlan plan;
+    if (!decode_plan(M, N, K, group, bits, zeros != nullptr, true, f->num_sms, f->smem_pair, f->smem_optin, &plan))
+        return QMM_ERR_UNSUPPORTED;
+    DecodeParams d;
+    std::memset(&d, 0, sizeof(d));
+    d.x = static_cast<const uint16_t *>(x);
+    d.packed = tiled;
+    d.scales = static_cast<const uint16_t *>(scales);
+    d.zeros = zeros;
+    d.y = y;
+    d.status = f->status;
+    d.row_bytes = static_cast<long long>(K) * bits / 8;
+    d.M = M;
+    d.N = N;
+    d.K = K;
+    d.group_log2 = group == 64 ? 6 : 7;
+    d.y_bf16 = y_dtype == QMM_BF16;
+    d.zero_const = zeros ? 0 : zero_const;
+    d.pl = plan;
+    return from_cuda(launch_decode(d, bits, true, stream));
 }
 
 qmm_status qmm_set_gemv_kernel(int kernel)

@@ -11,14 +11,14 @@ namespace qmm {
 // layout (byte offsets from the 128-byte aligned dynamic shared memory base).
 struct DecodePlan {
     int grid;                 // CTAs: min(N, SMs)
-    int rows_base, rows_rem;  // CTA c owns rows_base + (c < rows_rem) output columns
+    int rows_base, rows_rem;  // CTA c owns rows_base + (c < rows_rem) output columns (tile16: 16-row tiles)
     int max_rows;             // rows of the largest CTA
     int warps;                // warps per CTA (8)
     int kseg;                 // codes per K segment: one group per warp
     int nseg;                 // K / kseg
     int seg_bytes;            // kseg * b / 8: one row's bytes of one segment
     int span;                 // segments per ring slot: nseg (whole rows) or 1
-    int pitch;                // bytes between rows in a ring slot (padded)
+    int pitch;                // bytes between rows in a ring slot (padded; 0 for tile16)
     int slot_bytes;           // min(32, max_rows) * pitch
     int slots;                // ring depth: segments in flight
     int x_pitch;              // bytes per token of one warp's activation stage
@@ -42,10 +42,12 @@ struct DecodeParams {
 // Plans a call; false if the kernel does not take the shape (the skinny kernel
 // does).  smem_pair is the per-CTA shared memory with which two CTAs share an
 // SM, smem_optin the most one CTA may use.  Host code only.
-bool decode_plan(int M, int N, int K, int group, int bits, bool stored_zeros, int num_sms,
+bool decode_plan(int M, int N, int K, int group, int bits, bool stored_zeros, bool tile16, int num_sms,
                  int smem_pair, int smem_optin, DecodePlan *plan);
 
-// Launches the kernel for b = bits (1..8) with programmatic dependent launch.
-cudaError_t launch_decode(const DecodeParams &p, int bits, cudaStream_t stream);
+// Launches the kernel for b = bits (1..8) with programmatic dependent launch;
+// tile16: the weights are in the fragment-ordered layout (qmm_repack).
+cudaError_t launch_decode(const DecodeParams &p, int bits, bool tile16, cudaStream_t stream);
+cudaError_t launch_decode_tile16(const DecodeParams &p, int bits, cudaStream_t stream);
 
 }  // namespace qmm

@@ -70,6 +70,8 @@ cudaError_t launch_pack(const uint8_t *codes, uint8_t *packed, int N, int K, int
 cudaError_t launch_unpack(const uint8_t *packed, uint8_t *codes, int N, int K, int bits,
                           cudaStream_t stream, int num_sms);
 cudaError_t launch_flip_sign(uint8_t *packed, int N, int K, int bits, cudaStream_t stream, int num_sms);
+cudaError_t launch_repack(const uint8_t *packed, uint8_t *out, int N, int K, int bits, int layout,
+                          cudaStream_t stream, int num_sms);
 
 // Tensor maps (api.cu).  A 2-D map over a byte matrix [rows][row_bytes] with a
 // box_cols x box_rows box; and over a 16-bit matrix [rows][cols] with the

@@ -197,6 +197,49 @@ QMM_API qmm_status qmm_gemv_float(const void *x, const uint8_t *packed, int ebit
                                   int group, const void *scales, void *y, int M, int N, int K,
                                   cudaStream_t stream);
 
+/* Pre-permuted weight layouts, written offline from the packed bitstream
+ * (BitLLM sec. 4.3: weights are re-laid out ahead of time so that the kernel's
+ * loads need no reordering; Fig. 6 / Fig. 8(b) for the int4 order).
+ *   QMM_LAYOUT_TILE16 (any width): the fragment-ordered layout qmm_gemv_tile16
+ *     reads.  Rows in tiles of 16 (the last tile padded with zero codes), K in
+ *     blocks of 64 codes; unit (T, kb) is 128*bits bytes at byte
+ *     (T*(K/64) + kb)*128*bits, and holds run r = (h*8 + g)*4 + t -- codes
+ *     16t .. 16t+15 of the block for row 16T + 8h + g, LSB first -- at bytes
+ *     [2*bits*r, 2*bits*r + 2*bits).  Each run is the 16-code slice one
+ *     tensor-core thread reads, so a warp's reads are contiguous and a CTA's
+ *     share of the weights is a few large bulk copies.  Needs K % 64 == 0.
+ *     Size: ceil(N/16) * 16 * K * bits / 8 bytes.
+ *   QMM_LAYOUT_INTERLEAVE4 (bits == 4): BitLLM's lane-interleaved order: in
+ *     every 32-bit word the nibble slots hold codes 0 4 1 5 2 6 3 7 of the
+ *     word's eight, so W & 0x0F0F0F0F gives codes 0..3 and
+ *     (W >> 4) & 0x0F0F0F0F codes 4..7 as bytes.  Needs K % 8 == 0.
+ *     Size: N * K / 2 bytes.  (A format conversion; no kernel here reads it:
+ *     the fp16 operand extraction costs one shift and four LOP3s per word from
+ *     the canonical stream already.) */
+typedef enum { QMM_LAYOUT_TILE16 = 1, QMM_LAYOUT_INTERLEAVE4 = 2 } qmm_layout;
+
+/* Bytes of the `layout` form of an N x K `bits`-bit weight matrix, or 0 if the
+ * layout does not take these sizes. */
+QMM_API size_t qmm_repack_bytes(int N, int K, int bits, int layout);
+
+/* packed (device) [N][K*bits/8] canonical bitstream -> out (device,
+ * qmm_repack_bytes(N, K, bits, layout) bytes, fully overwritten) in `layout`.
+ * Byte-exact; an offline step like qmm_pack.  Errors: QMM_ERR_BITS,
+ * QMM_ERR_SHAPE (sizes the layout does not take), QMM_ERR_NULL,
+ * QMM_ERR_DEVICE, QMM_ERR_CUDA. */
+QMM_API qmm_status qmm_repack(const uint8_t *packed, uint8_t *out, int N, int K, int bits, int layout,
+                              cudaStream_t stream);
+
+/* qmm_gemv on weights in the QMM_LAYOUT_TILE16 layout (`tiled`, 16-byte
+ * aligned; everything else as for qmm_gemv).  Served by the decode kernel
+ * only: shapes it does not take (M > 16, G = 32, K not a multiple of 8
+ * groups, activations too large for shared memory) return
+ * QMM_ERR_UNSUPPORTED.  Results equal qmm_gemv's on the canonical stream up
+ * to the order of the fp32 sums. */
+QMM_API qmm_status qmm_gemv_tile16(const void *x, qmm_dtype x_dtype, const uint8_t *tiled, int bits,
+                                   int group, const void *scales, const uint8_t *zeros, int zero_const,
+                                   void *y, qmm_dtype y_dtype, int M, int N, int K, cudaStream_t stream);
+
 /* Signed b-bit weights.  Flips, in place, the top bit of every b-bit code of
  * a packed stream [N][K*bits/8] (two's complement <-> offset binary).  A
  * stream of signed codes c (w = c * s, the signed integer types among the

@@ -21,14 +21,15 @@ def lib():
 
 def declared_symbols():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^QMM_API (?:qmm_status|const char \*|int)\s*(qmm_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^QMM_API (?:qmm_status|const char \*|int|size_t)\s*(qmm_\w+)\s*\(", text, re.M)))
 
 
 def test_header_declares_the_calls():
     syms = declared_symbols()
     for name in ("qmm_pack", "qmm_unpack", "qmm_gemv", "qmm_gemm", "qmm_w4a8", "qmm_w8a8",
                  "qmm_quantize_act", "qmm_flip_sign", "qmm_gemv_float", "qmm_set_gemv_kernel",
-                 "qmm_gemv_route", "qmm_device_status", "qmm_status_string", "qmm_abi_version"):
+                 "qmm_gemv_route", "qmm_repack", "qmm_repack_bytes", "qmm_gemv_tile16",
+                 "qmm_device_status", "qmm_status_string", "qmm_abi_version"):
         assert name in syms
 
 
@@ -103,6 +104,20 @@ def test_gemv_route_rejects_bad_shapes(lib):
     assert lib.qmm_gemv_route(1, 64, 512, 9, 128, 0) == -3      # bits
     assert lib.qmm_gemv_route(1, 64, 500, 4, 128, 0) == -3      # K % group
     assert lib.qmm_gemv_route(1, 64, 512, 4, 48, 0) == -3       # group
+
+
+def test_repack_sizes_and_argument_errors(lib):
+    lib.qmm_repack_bytes.restype = ctypes.c_size_t
+    assert lib.qmm_repack_bytes(37, 128, 3, 1) == 48 * 128 * 3 // 8     # tile16 pads rows to 16
+    assert lib.qmm_repack_bytes(37, 96, 3, 1) == 0                      # K % 64
+    assert lib.qmm_repack_bytes(37, 96, 4, 2) == 37 * 48                # interleave4
+    assert lib.qmm_repack_bytes(37, 96, 3, 2) == 0                      # interleave4 is 4-bit only
+    assert lib.qmm_repack(A16, B16, 4, 96, 4, 1, None) == 3             # K % 64
+    assert lib.qmm_repack(A16, B16, 4, 64, 9, 1, None) == 2             # bits
+    assert lib.qmm_repack(None, B16, 4, 64, 4, 1, None) == 1
+    assert lib.qmm_repack(A16, B16, 4, 64, 4, 7, None) == 3             # layout
+    # the tile16 gemv needs a 16-byte aligned stream
+    assert lib.qmm_gemv_tile16(A16, 0, _fake(0x20004), 4, 128, A16, None, 8, B16, 0, 1, 64, 128, None) == 4
 
 
 def test_gemv_float_argument_errors(lib):

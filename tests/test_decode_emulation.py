@@ -205,7 +205,7 @@ def _code_exps(b):
     return e
 
 
-def _emulate_staged(prob, packed, plan):
+def _emulate_staged(prob, packed, plan, tile16=False):
     """y of the staged decode kernel, emulated from its plan: bulk copies place each
     row's chunk in a ring slot at the plan's pitch; each warp stages its group of
     every segment in fragment (slot) order and forms X and C per group; every lane
@@ -229,8 +229,10 @@ def _emulate_staged(prob, packed, plan):
     slot_code = _slot_codes(b)
     y = np.zeros((M, N))
     for cta in range(plan["grid"]):
-        r0 = cta * plan["rows_base"] + min(cta, plan["rows_rem"])
-        nrows = plan["rows_base"] + (1 if cta < plan["rows_rem"] else 0)
+        u0 = cta * plan["rows_base"] + min(cta, plan["rows_rem"])
+        nu = plan["rows_base"] + (1 if cta < plan["rows_rem"] else 0)
+        r0 = 16 * u0 if tile16 else u0
+        nrows = min(16 * nu, N - r0) if tile16 else nu
         sm = np.zeros(plan["smem"], dtype=np.uint8)
         # scales / zeros of the CTA's rows, transposed to [group][row]
         sc = np.zeros(ng * nrows, dtype=np.uint16)
@@ -272,7 +274,14 @@ def _emulate_staged(prob, packed, plan):
                 i = rb * (nseg // span) + c
                 slot = i % S
                 base = slot * slot_bytes
-                if jj == 0:   # the chunk's bulk copies: one per row
+                if jj == 0 and tile16:   # the chunk's bulk copies: one per 16-row tile
+                    for ti in range(-(-cnt // 16)):
+                        dst = base + ti * 16 * chunk
+                        assert dst + 16 * chunk <= base + slot_bytes <= plan["off_x"]
+                        src = (r0 + rr) * row_bytes + c * 16 * chunk + ti * 16 * row_bytes
+                        assert src + 16 * chunk <= packed.size
+                        sm[dst:dst + 16 * chunk] = packed.reshape(-1)[src:src + 16 * chunk]
+                elif jj == 0:   # the chunk's bulk copies: one per row
                     for r in range(cnt):
                         dst = base + r * pitch
                         assert dst + chunk <= base + slot_rows * pitch <= plan["off_x"]
@@ -291,9 +300,16 @@ def _emulate_staged(prob, packed, plan):
                                     for h in range(2):
                                         row = 16 * i2 + 8 * h + g
                                         lr = min(row, cnt - 1)
-                                        a = (base + lr * pitch + jj * plan["seg_bytes"] + (64 * (w * NB + bb)) * b // 8
-                                             + first_b)
-                                        assert base <= a and a + 4 * nw <= base + lr * pitch + (jj + 1) * plan["seg_bytes"]
+                                        kblock = jj * (kseg // 64) + w * NB + bb
+                                        if tile16:   # the padding rows of a tile are real zero codes
+                                            a = (base + i2 * 16 * chunk + kblock * 128 * b + ((8 * h + g) * 4 + t) * 2 * b
+                                                 - (2 if (b & 1) and (t & 1) else 0))
+                                            assert base <= a and a + 4 * nw <= base + slot_bytes
+                                            if row >= cnt:
+                                                continue
+                                        else:
+                                            a = base + lr * pitch + kblock * 8 * b + first_b
+                                            assert base <= a and a + 4 * nw <= base + lr * pitch + (jj + 1) * plan["seg_bytes"]
                                         if b == 4:
                                             assert a % 8 == 0
                                         if b == 8:
@@ -338,6 +354,24 @@ def test_staged_kernel_emulation_matches_oracle(b, M, N, K, G, zm, sms, tmp_path
     assert plan is not None
     packed, _ = oracle.pack(prob.codes, b)
     y = _emulate_staged(prob, packed, plan)
+    ref = oracle.solve_qmm(prob)
+    np.testing.assert_allclose(y, ref, rtol=0, atol=1e-9 * max(1.0, np.abs(ref).max()))
+
+
+@pytest.mark.parametrize("b,M,N,K,G,zm,sms", [
+    (4, 1, 40, 1024, 128, "half", 2), (3, 3, 75, 1024, 64, "group", 2), (8, 2, 37, 2048, 128, "group", 1),
+    (7, 9, 20, 512, 64, "const8", 1), (5, 1, 8, 2048, 64, "group", 4)])
+def test_staged_kernel_emulation_tile16(b, M, N, K, G, zm, sms, tmp_path):
+    # the fragment-ordered layout (written by the oracle's tile16): one bulk copy
+    # per tile, runs read at their tile16 offsets
+    import oracle
+    import synthetic
+    from tests.test_planner import SMEM_OPTIN, SMEM_PAIR, decode_plans
+    prob = synthetic.make_qmm(M, N, K, b, G, zero_mode=zm, seed=b + 7 * M)
+    plan = decode_plans([(M, N, K, G, b, 1 if prob.zeros is not None else 0, sms, SMEM_PAIR, SMEM_OPTIN, 1)],
+                        tmp_path)[0]
+    assert plan is not None
+    y = _emulate_staged(prob, oracle.tile16(prob.codes, b), plan, tile16=True)
     ref = oracle.solve_qmm(prob)
     np.testing.assert_allclose(y, ref, rtol=0, atol=1e-9 * max(1.0, np.abs(ref).max()))
 

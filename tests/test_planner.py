@@ -8,7 +8,7 @@ limit, and fit the decode shapes in half an SM (two CTAs per SM, so that
 consecutive calls overlap).
 
 tests/decode_route_check.cu does the same for the decode kernel's shape rule
-(bit_weight_quantized_gb300/csrc/decode.cu, decode_supports), checked against
+and launch plan (bit_weight_quantized_gb300/csrc/decode.cu, decode_plan), checked against
 the rule as documented for qmm_gemv.
 """
 import json
@@ -128,8 +128,9 @@ SMEM_PAIR, SMEM_OPTIN = 115712, 232448   # GB300: half an SM's shared memory per
 
 
 def decode_plans(shapes, tmp_dir):
-    """Runs tests/decode_route_check.cu on (M, N, K, G, bits, zeros, sms, pair, optin)
-    tuples; returns None (skinny kernel) or a dict of the DecodePlan per shape."""
+    """Runs tests/decode_route_check.cu on (M, N, K, G, bits, zeros, sms, pair, optin
+    [, tile16]) tuples; returns None (skinny kernel) or a dict of the DecodePlan per
+    shape."""
     nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
     if not os.path.exists(nvcc):
         pytest.skip("nvcc not available")
@@ -138,12 +139,12 @@ def decode_plans(shapes, tmp_dir):
         subprocess.run([nvcc, "-std=c++17", "-O1", "-gencode", "arch=compute_103a,code=sm_103a",
                         "--expt-relaxed-constexpr", "-o", exe, os.path.join(HERE, "decode_route_check.cu")],
                        check=True, capture_output=True)
-    stdin = "".join(" ".join(map(str, sh)) + "\n" for sh in shapes)
+    stdin = "".join(" ".join(map(str, sh[:9])) + f" {sh[9] if len(sh) > 9 else 0}\n" for sh in shapes)
     out = subprocess.run([exe], input=stdin, capture_output=True, text=True, check=True).stdout
     res = []
     for line, sh in zip(out.splitlines(), shapes):
         v = list(map(int, line.split()))
-        assert tuple(v[:9]) == tuple(sh)
+        assert tuple(v[:9]) == tuple(sh[:9])
         res.append(dict(zip(DECODE_FIELDS, v[10:])) if v[9] else None)
     assert len(res) == len(shapes)
     return res
@@ -233,3 +234,25 @@ def test_decode_sweep_keeps_two_ctas_per_sm_and_preloads(dplans):
                 assert pl["span"] == pl["nseg"] and pl["slots"] == 1, b
             else:
                 assert pl["span"] == 1 and pl["slots"] * 4 >= pl["nseg"] * 3, b
+
+
+def test_decode_plan_tile16_layout(tmp_path_factory):
+    # the fragment-ordered layout: CTAs own whole 16-row tiles, slots hold two
+    # dense tiles, everything else as for the canonical layout
+    shapes = [(M, N, K, G, b, z, sms, SMEM_PAIR, SMEM_OPTIN, 1)
+              for sms in (152, 4) for b in (1, 3, 4, 8) for M in (1, 9, 16)
+              for (N, K, G, z) in [(4096, 4096, 128, 0), (14336, 4096, 64, 1), (37, 1024, 128, 1), (8, 2048, 64, 0)]]
+    plans = decode_plans(shapes, tmp_path_factory.mktemp("tile"))
+    for sh, pl in zip(shapes, plans):
+        M, N, K, G, b, z, sms = sh[:7]
+        if pl is None:
+            continue
+        tiles = -(-N // 16)
+        assert pl["grid"] == min(tiles, sms), sh
+        assert pl["grid"] * pl["rows_base"] + pl["rows_rem"] == tiles, sh
+        assert pl["max_rows"] == min(16 * (pl["rows_base"] + (pl["rows_rem"] > 0)), N), sh
+        assert pl["pitch"] == 0 and pl["slot_bytes"] == 32 * pl["span"] * pl["seg_bytes"], sh
+        assert pl["slots"] * pl["slot_bytes"] <= pl["off_x"] and pl["smem"] <= SMEM_OPTIN, sh
+    sweep = {sh[4]: pl for sh, pl in zip(shapes, plans) if sh[:4] == (1, 4096, 4096, 128) and sh[6] == 152}
+    for b in (1, 3, 4):
+        assert sweep[b]["span"] == sweep[b]["nseg"] and sweep[b]["smem"] <= SMEM_PAIR, b
