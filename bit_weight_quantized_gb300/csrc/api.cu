@@ -313,6 +313,7 @@ qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int
         d.group_log2 = group == 64 ? 6 : 7;
         d.y_bf16 = y_dtype == QMM_BF16;
         d.zero_const = zeros ? 0 : zero_const;
+        d.vec_sz = aligned(scales, 16) && (!zeros || aligned(zeros, 8));
         d.pl = plan;
         return from_cuda(launch_decode(d, bits, false, stream));
     }
@@ -436,6 +437,7 @@ qmm_status qmm_gemv_tile16(const void *x, qmm_dtype x_dtype, const uint8_t *tile
     d.group_log2 = group == 64 ? 6 : 7;
     d.y_bf16 = y_dtype == QMM_BF16;
     d.zero_const = zeros ? 0 : zero_const;
+    d.vec_sz = aligned(scales, 16) && (!zeros || aligned(zeros, 8));
     d.pl = plan;
     return from_cuda(launch_decode(d, bits, true, stream));
 }

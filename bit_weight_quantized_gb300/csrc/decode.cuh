@@ -154,10 +154,11 @@ __device__ __forceinline__ void issue_chunk(const DecodeParams &p, uint8_t *slot
 
 // One warp's 64-code block: the thread's runs of its four rows turned into
 // exact code pairs, its activation fragments (already in pair order), and the
-// MMAs into the group accumulators.
+// MMAs into the group accumulators.  MMAs j = 0, 2 and j = 1, 3 go to separate
+// accumulator sets (summed at the fold), which halves the dependent chains.
 template <int B, int NT>
 __device__ __forceinline__ void block_mma(const uint8_t *const (&run0)[2][2], int boff, const uint8_t *xb,
-                                          int x_pitch, int m0, int m1, int o, float (&acc)[2][NT][4])
+                                          int x_pitch, int m0, int m1, int o, float (&acc)[2][2][NT][4])
 {
     constexpr int NW = run_words<B>();
     uint32_t a[2][2][8];
@@ -185,7 +186,7 @@ __device__ __forceinline__ void block_mma(const uint8_t *const (&run0)[2][2], in
         for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int tt = 0; tt < NT; ++tt)
-                mma_f16_16816(acc[i][tt], a[i][0][2 * j], a[i][1][2 * j], a[i][0][2 * j + 1],
+                mma_f16_16816(acc[j & 1][i][tt], a[i][0][2 * j], a[i][1][2 * j], a[i][0][2 * j + 1],
                               a[i][1][2 * j + 1], xw[tt][2 * j], xw[tt][2 * j + 1]);
 }
 
@@ -268,7 +269,7 @@ __device__ __noinline__ void stage_rounds(const DecodeParams &p, uint8_t *xw, fl
 // NB = G / 64 blocks per group; warp w owns group w of every 8-group segment.
 // TILE: the weights are in the fragment-ordered (tile16) layout.
 template <int B, int NT, int NB, bool TILE>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
 decode_kernel(const DecodeParams p)
 {
     const DecodePlan &pl = p.pl;
@@ -316,7 +317,37 @@ decode_kernel(const DecodeParams p)
     }
     // the CTA's scales and zeros (fp16) into shared memory, transposed to
     // [group][row] so that the eight rows of a fragment meet consecutive halves
-    {
+    if (p.vec_sz) {
+        // eight groups of a row per step: one 16-byte load of scales and one
+        // 8-byte load of zeros; (row, c) advance by a fixed stride without divisions
+        const int vpr = ng >> 3;                        // 8-group vectors per row
+        const int total = nrows * vpr;
+        const int dq = kThreads / vpr, dr = kThreads - dq * vpr;
+        int row = threadIdx.x / vpr, c = threadIdx.x - row * vpr;
+        const uint4 *gs = reinterpret_cast<const uint4 *>(p.scales + static_cast<long long>(r0) * ng);
+        const uint2 *gz = reinterpret_cast<const uint2 *>(p.zeros + static_cast<long long>(r0) * ng);
+        for (int v = threadIdx.x; v < total; v += kThreads) {
+            const uint4 sv = gs[v];
+            const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+            uint16_t *sd = sc + 8 * c * nrows + row;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                sd[e * nrows] = static_cast<uint16_t>(sw[e >> 1] >> (16 * (e & 1)));
+            if (p.zeros) {
+                const uint2 zv = gz[v];
+                uint16_t *zd = zo + 8 * c * nrows + row;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    zd[e * nrows] = f32_to_f16_bits(static_cast<float>(((e < 4 ? zv.x : zv.y) >> (8 * (e & 3))) & 0xFFu));
+            }
+            row += dq;
+            c += dr;
+            if (c >= vpr) {
+                c -= vpr;
+                ++row;
+            }
+        }
+    } else {
         const uint16_t *gs = p.scales + static_cast<long long>(r0) * ng;
         for (int e = threadIdx.x; e < nrows * ng; e += kThreads) {
             const int row = e / ng, gi = e - row * ng;
@@ -419,14 +450,16 @@ decode_kernel(const DecodeParams p)
 #pragma unroll 1
                 for (int jj = 0; jj < pl.span; ++jj) {
                     const int j = c * pl.span + jj;
-                    float acc[2][NT][4];
+                    float acc[2][2][NT][4];
 #pragma unroll
-                    for (int i = 0; i < 2; ++i)
+                    for (int u = 0; u < 2; ++u)
 #pragma unroll
-                        for (int tt = 0; tt < NT; ++tt)
+                        for (int i = 0; i < 2; ++i)
 #pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                acc[i][tt][e] = 0.f;
+                            for (int tt = 0; tt < NT; ++tt)
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    acc[u][i][tt][e] = 0.f;
 #pragma unroll
                     for (int bb = 0; bb < NB; ++bb) {
                         // block kblock of the chunk: 8 b bytes apart per row (canonical), or one
@@ -459,7 +492,8 @@ decode_kernel(const DecodeParams p)
 #pragma unroll
                                 for (int cc = 0; cc < 2; ++cc)
                                     tot[i][tt][2 * h + cc] = fmaf(
-                                        s, fmaf(-z, X[tt][cc], acc[i][tt][2 * h + cc] - D[tt][cc]), tot[i][tt][2 * h + cc]);
+                                        s, fmaf(-z, X[tt][cc], (acc[0][i][tt][2 * h + cc] + acc[1][i][tt][2 * h + cc]) - D[tt][cc]),
+                                    tot[i][tt][2 * h + cc]);
                         }
                 }
             }

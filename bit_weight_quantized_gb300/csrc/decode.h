@@ -36,6 +36,7 @@ struct DecodeParams {
     long long row_bytes;      // K * b / 8
     int M, N, K, group_log2, y_bf16;
     int zero_const;           // the zero of every group when zeros == nullptr
+    int vec_sz;               // scales 16-byte and zeros 8-byte aligned: vector staging
     DecodePlan pl;
 };
 
