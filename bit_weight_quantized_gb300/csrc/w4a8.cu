@@ -25,6 +25,8 @@ qmm_status wxa8_dispatch(int bits, const int8_t *xq, const void *sa, const uint8
                          int group, void *y, int32_t *acc_out, int M, int N, int K, int *status,
                          int num_sms, int smem_optin, int smem_pair, cudaStream_t stream)
 {
+    if (M >= (bits == 8 ? kW8a8TcMinM : kW4a8TcMinM) && wxa8_tc_takes(bits, M, N, K, group, xq, w))
+        return wxa8_tc_dispatch(bits, xq, sa, w, ws, group, y, acc_out, M, N, K, status, smem_optin, stream);
     GemvParams p;
     std::memset(&p, 0, sizeof(p));
     p.xq = xq;

@@ -13,4 +13,14 @@ qmm_status wxa8_dispatch(int bits, const int8_t *xq, const void *sa, const uint8
                          int group, void *y, int32_t *acc_out, int M, int N, int K, int *status,
                          int num_sms, int smem_optin, int smem_pair, cudaStream_t stream);
 
+// The tcgen05 path (wxa8_tc.cu): whether it takes the shape, and its launch.
+// Below these batch sizes the skinny kernel is faster (measured: W4A8 up to
+// M = 4, W8A8 at M = 1).
+constexpr int kW4a8TcMinM = 6;
+constexpr int kW8a8TcMinM = 2;
+bool wxa8_tc_takes(int bits, int M, int N, int K, int group, const void *xq, const void *w);
+qmm_status wxa8_tc_dispatch(int bits, const int8_t *xq, const void *sa, const uint8_t *w, const void *ws,
+                            int group, void *y, int32_t *acc_out, int M, int N, int K, int *status,
+                            int smem_optin, cudaStream_t stream);
+
 }  // namespace qmm

@@ -174,7 +174,13 @@ QMM_API qmm_status qmm_gemm(const void *x, qmm_dtype x_dtype, const uint8_t *pac
  *   ws      (device) fp16 [N][K/G] per-group weight scales, G in {32, 64, 128}.
  *   y       (device) fp16 [M][N].
  *   acc_out (device, may be NULL) int32 [M][N][K/G]: the integer accumulators.
- * Requires 1 <= M <= 64 (decode and small batches), K % G == 0. */
+ * Requires 1 <= M <= 64 (decode and small batches), K % G == 0.
+ * Two kernels serve it.  For M >= 6 with K a multiple of 512 and K/G/4 <= 32
+ * (and xq, w4 16-byte aligned) a tcgen05 kernel runs: weights and activations
+ * become exact fp16 operands, each group accumulates in its own tensor-memory
+ * accumulator (every product and sum is an integer below 2^24, so the fp32
+ * accumulation is exact), and a cluster of four CTAs splits K.  Other shapes
+ * take the skinny kernel (fp16 mma.sync on the same exact operands). */
 QMM_API qmm_status qmm_w4a8(const int8_t *xq, const void *sa, const uint8_t *w4, const void *ws,
                     int group, void *y, int32_t *acc_out, int M, int N, int K,
                     cudaStream_t stream);
@@ -259,7 +265,9 @@ QMM_API qmm_status qmm_flip_sign(uint8_t *packed, int N, int K, int bits, cudaSt
  *        aligned.  Everything else as for qmm_w4a8:
  *   acc[m][n][g] = sum_{k in g} xq[m][k] * w8[n][k]   (exact int32)
  *   y[m][n]      = sa[m] * sum_g ws[n][g] * acc[m][n][g]   (fp32 -> fp16 RNE)
- * 1 <= M <= 64, G in {32, 64, 128}.  Errors as for qmm_w4a8. */
+ * 1 <= M <= 64, G in {32, 64, 128}.  Errors as for qmm_w4a8.  The tcgen05
+ * kernel of qmm_w4a8 serves M >= 2 under the same conditions on K (|acc| <=
+ * 128 * 128 * G stays exact), the skinny kernel the rest. */
 QMM_API qmm_status qmm_w8a8(const int8_t *xq, const void *sa, const int8_t *w8, const void *ws,
                             int group, void *y, int32_t *acc_out, int M, int N, int K,
                             cudaStream_t stream);
