@@ -670,6 +670,51 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+PROFILE_FAMILIES = ("skinny_tile16_m16", "w4a8_m64", "tiled_m128")
+
+
+def run_profile_family(name: str, launches: int = 4):
+    """A few eager calls of one workload family on device-generated inputs, for
+    a profiler to capture one of them: the skinny batched decode on the
+    fragment-ordered layout (M = 16, N = 14336, K = 4096, b = 6, group 64,
+    stored zeros), W4A8 at M = 64 (K = N = 4096, group 128) or the tiled path at
+    M = 128 (K = 8192, N = 28672, int4, bf16)."""
+    import torch
+    import bit_weight_quantized_gb300 as q
+    q.load()
+    dev = torch.device("cuda:0")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    if name == "skinny_tile16_m16":
+        M, N, K, b, G = 16, 14336, 4096, 6, 64
+        tiled = q.qmm_repack(q.qmm_pack(torch.randint(0, 1 << b, (N, K), dtype=torch.uint8, device=dev,
+                                                      generator=gen), b), K, b, "tile16")
+        sc = (0.02 * torch.randn(N, K // G, device=dev, generator=gen).abs() + 1e-3).half()
+        zz = torch.randint(0, 1 << b, (N, K // G), dtype=torch.uint8, device=dev, generator=gen)
+        x = torch.randn(M, K, device=dev, generator=gen).half()
+        call = lambda: q.qmm_gemv_tile16(x, tiled, N, b, G, sc, zz)
+    elif name == "w4a8_m64":
+        M, N, K = 64, 4096, 4096
+        w = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=dev, generator=gen)
+        ws = (0.02 * torch.randn(N, K // 128, device=dev, generator=gen).abs() + 1e-3).half()
+        xq = torch.randint(-127, 128, (M, K), dtype=torch.int8, device=dev, generator=gen)
+        sa = (0.02 * torch.randn(M, device=dev, generator=gen).abs() + 1e-3).half()
+        call = lambda: q.qmm_w4a8(xq, sa, w, ws, 128)
+    else:
+        M, N, K = 128, 28672, 8192
+        w = q.qmm_pack(torch.randint(0, 16, (N, K), dtype=torch.uint8, device=dev, generator=gen), 4)
+        sc = (0.02 * torch.randn(N, K // 128, device=dev, generator=gen).abs() + 1e-3).half()
+        x = torch.randn(M, K, device=dev, generator=gen).bfloat16()
+        call = lambda: q.qmm_gemm(x, w, 4, 128, sc, None, 8)
+    for _ in range(launches):
+        call()
+    torch.cuda.synchronize()
+    st = q.qmm_device_status()
+    if st:
+        raise SystemExit(f"device status {st}")
+    print(json.dumps({"profile": name, "launches": launches}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -683,7 +728,12 @@ def main():
     ap.add_argument("--gemv-kernel", choices=["auto", "skinny"], default="auto",
                     help="qmm_gemv's kernel: the default choice, or the skinny kernel forced "
                          "for every shape (for profiling that kernel on the sweep)")
+    ap.add_argument("--profile", choices=PROFILE_FAMILIES,
+                    help="run four eager calls of one workload family and exit (for a profiler)")
     args = ap.parse_args()
+    if args.profile:
+        run_profile_family(args.profile)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world, rank, local = dist_setup()

@@ -154,8 +154,10 @@ __device__ __forceinline__ void issue_chunk(const DecodeParams &p, uint8_t *slot
 
 // One warp's 64-code block: the thread's runs of its four rows turned into
 // exact code pairs, its activation fragments (already in pair order), and the
-// MMAs into the group accumulators.  MMAs j = 0, 2 and j = 1, 3 go to separate
-// accumulator sets (summed at the fold), which halves the dependent chains.
+// MMAs into the group accumulators.  With two token tiles (NT = 2, one CTA per
+// SM) MMAs j = 0, 2 and j = 1, 3 go to separate accumulator sets (summed at
+// the fold), which halves the dependent chains; with one (two CTAs per SM, 128
+// registers) a single set measured faster.
 template <int B, int NT>
 __device__ __forceinline__ void block_mma(const uint8_t *const (&run0)[2][2], int boff, const uint8_t *xb,
                                           int x_pitch, int m0, int m1, int o, float (&acc)[2][2][NT][4])
@@ -186,7 +188,7 @@ __device__ __forceinline__ void block_mma(const uint8_t *const (&run0)[2][2], in
         for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int tt = 0; tt < NT; ++tt)
-                mma_f16_16816(acc[j & 1][i][tt], a[i][0][2 * j], a[i][1][2 * j], a[i][0][2 * j + 1],
+                mma_f16_16816(acc[NT == 2 ? (j & 1) : 0][i][tt], a[i][0][2 * j], a[i][1][2 * j], a[i][0][2 * j + 1],
                               a[i][1][2 * j + 1], xw[tt][2 * j], xw[tt][2 * j + 1]);
 }
 
@@ -317,9 +319,11 @@ decode_kernel(const DecodeParams p)
     }
     // the CTA's scales and zeros (fp16) into shared memory, transposed to
     // [group][row] so that the eight rows of a fragment meet consecutive halves
-    if (p.vec_sz) {
+    if (NT == 2 && p.vec_sz) {
         // eight groups of a row per step: one 16-byte load of scales and one
-        // 8-byte load of zeros; (row, c) advance by a fixed stride without divisions
+        // 8-byte load of zeros; (row, c) advance by a fixed stride without
+        // divisions (the one-token-tile variant keeps the smaller scalar loop:
+        // there the staging overlaps the preceding call, and the code size shows)
         const int vpr = ng >> 3;                        // 8-group vectors per row
         const int total = nrows * vpr;
         const int dq = kThreads / vpr, dr = kThreads - dq * vpr;
@@ -492,7 +496,8 @@ decode_kernel(const DecodeParams p)
 #pragma unroll
                                 for (int cc = 0; cc < 2; ++cc)
                                     tot[i][tt][2 * h + cc] = fmaf(
-                                        s, fmaf(-z, X[tt][cc], (acc[0][i][tt][2 * h + cc] + acc[1][i][tt][2 * h + cc]) - D[tt][cc]),
+                                        s, fmaf(-z, X[tt][cc], (NT == 2 ? acc[0][i][tt][2 * h + cc] + acc[1][i][tt][2 * h + cc]
+                                                                        : acc[0][i][tt][2 * h + cc]) - D[tt][cc]),
                                     tot[i][tt][2 * h + cc]);
                         }
                 }

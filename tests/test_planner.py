@@ -127,6 +127,9 @@ DECODE_FIELDS = ("grid", "rows_base", "rows_rem", "max_rows", "warps", "kseg", "
 SMEM_PAIR, SMEM_OPTIN = 115712, 232448   # GB300: half an SM's shared memory per CTA, and the opt-in limit
 
 
+_DECODE_EXE = {}
+
+
 def decode_plans(shapes, tmp_dir):
     """Runs tests/decode_route_check.cu on (M, N, K, G, bits, zeros, sms, pair, optin
     [, tile16]) tuples; returns None (skinny kernel) or a dict of the DecodePlan per
@@ -134,11 +137,13 @@ def decode_plans(shapes, tmp_dir):
     nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
     if not os.path.exists(nvcc):
         pytest.skip("nvcc not available")
-    exe = os.path.join(str(tmp_dir), "decode_route_check")
-    if not os.path.exists(exe):
+    exe = _DECODE_EXE.get("path")
+    if exe is None:   # compiled once per test process (the kernels make it slow to build)
+        exe = os.path.join(str(tmp_dir), "decode_route_check")
         subprocess.run([nvcc, "-std=c++17", "-O1", "-gencode", "arch=compute_103a,code=sm_103a",
                         "--expt-relaxed-constexpr", "-o", exe, os.path.join(HERE, "decode_route_check.cu")],
                        check=True, capture_output=True)
+        _DECODE_EXE["path"] = exe
     stdin = "".join(" ".join(map(str, sh[:9])) + f" {sh[9] if len(sh) > 9 else 0}\n" for sh in shapes)
     out = subprocess.run([exe], input=stdin, capture_output=True, text=True, check=True).stdout
     res = []
