@@ -285,7 +285,7 @@ qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int
         return st;
     if (M > 16)
         return QMM_ERR_SHAPE;
-    if (x_dtype != QMM_F16 || (y_dtype != QMM_F16 && y_dtype != QMM_BF16))
+    if ((x_dtype != QMM_F16 && x_dtype != QMM_BF16) || (y_dtype != QMM_F16 && y_dtype != QMM_BF16))
         return QMM_ERR_UNSUPPORTED;
     if (M == 0 || N == 0)
         return QMM_OK;
@@ -312,12 +312,15 @@ qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int
         d.K = K;
         d.group_log2 = group == 64 ? 6 : 7;
         d.y_bf16 = y_dtype == QMM_BF16;
+        d.x_bf16 = x_dtype == QMM_BF16;
         d.zero_const = zeros ? 0 : zero_const;
         d.vec_sz = aligned(scales, 16) && (!zeros || aligned(zeros, 8));
         d.pl = plan;
         return from_cuda(launch_decode(d, bits, false, stream));
     }
 
+    if (x_dtype != QMM_F16)   // the skinny kernel stages fp16 activations only
+        return QMM_ERR_UNSUPPORTED;
     GemvParams p;
     std::memset(&p, 0, sizeof(p));
     p.x = static_cast<const uint16_t *>(x);
@@ -408,7 +411,7 @@ qmm_status qmm_gemv_tile16(const void *x, qmm_dtype x_dtype, const uint8_t *tile
         return st;
     if (M > 16)
         return QMM_ERR_SHAPE;
-    if (x_dtype != QMM_F16 || (y_dtype != QMM_F16 && y_dtype != QMM_BF16))
+    if ((x_dtype != QMM_F16 && x_dtype != QMM_BF16) || (y_dtype != QMM_F16 && y_dtype != QMM_BF16))
         return QMM_ERR_UNSUPPORTED;
     if (M == 0 || N == 0)
         return QMM_OK;
@@ -436,6 +439,7 @@ qmm_status qmm_gemv_tile16(const void *x, qmm_dtype x_dtype, const uint8_t *tile
     d.K = K;
     d.group_log2 = group == 64 ? 6 : 7;
     d.y_bf16 = y_dtype == QMM_BF16;
+    d.x_bf16 = x_dtype == QMM_BF16;
     d.zero_const = zeros ? 0 : zero_const;
     d.vec_sz = aligned(scales, 16) && (!zeros || aligned(zeros, 8));
     d.pl = plan;

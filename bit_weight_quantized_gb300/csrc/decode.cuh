@@ -197,9 +197,21 @@ __device__ __forceinline__ void block_mma(const uint8_t *const (&run0)[2][2], in
 // code_of_slot(s).  Returns the run's sums X = sum x and C = sum 2^E x (E of
 // each code's position in the plan), in fp32.
 template <int B>
-__device__ __forceinline__ float2 stage_run(uint8_t *dst, const uint4 (&raw)[2])
+__device__ __forceinline__ float2 stage_run(uint8_t *dst, const uint4 (&raw)[2], bool x_bf16)
 {
-    const uint32_t in[8] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w};
+    uint32_t in[8] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w};
+    if (x_bf16) {
+        // bf16 activations become fp16: exact for magnitudes in [2^-14, 65504]
+        // (8 significant bits fit in 11), rounded to the fp16 subnormal grid below
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            uint32_t h;
+            asm("cvt.rn.f16x2.f32 %0, %1, %2;"
+                : "=r"(h)
+                : "f"(__uint_as_float(in[q] & 0xFFFF0000u)), "f"(__uint_as_float(in[q] << 16)));
+            in[q] = h;
+        }
+    }
     uint32_t out[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
@@ -256,7 +268,8 @@ __device__ __noinline__ void stage_rounds(const DecodeParams &p, uint8_t *xw, fl
                     break;
                 float2 v = make_float2(0.f, 0.f);
                 if (jq[q] < pl.nseg)
-                    v = stage_run<B>(xw + mq[q] * pl.x_pitch + ((jq[q] * NB + bb) * 64 + 16 * tq) * 2, raw[q]);
+                    v = stage_run<B>(xw + mq[q] * pl.x_pitch + ((jq[q] * NB + bb) * 64 + 16 * tq) * 2, raw[q],
+                                     p.x_bf16 != 0);
 #pragma unroll
                 for (int off = 1; off < 4 * NB; off <<= 1) {
                     v.x += __shfl_xor_sync(0xffffffffu, v.x, off);
@@ -389,7 +402,7 @@ decode_kernel(const DecodeParams p)
                 const uint16_t *src = p.x + jl * pl.kseg + 64 * (warp * NB + bb) + 16 * tq;
                 const uint4 raw[2] = {*reinterpret_cast<const uint4 *>(src),
                                       *reinterpret_cast<const uint4 *>(src + 8)};
-                v = stage_run<B>(xw + ((jl * NB + bb) * 64 + 16 * tq) * 2, raw);
+                v = stage_run<B>(xw + ((jl * NB + bb) * 64 + 16 * tq) * 2, raw, p.x_bf16 != 0);
             }
 #pragma unroll
             for (int off = 1; off < 4 * NB; off <<= 1) {

@@ -27,7 +27,7 @@ struct DecodePlan {
 };
 
 struct DecodeParams {
-    const uint16_t *x;        // fp16 [M][K], 16-byte aligned
+    const uint16_t *x;        // fp16 or bf16 [M][K], 16-byte aligned
     const uint8_t *packed;    // [N][K*b/8], 16-byte aligned
     const uint16_t *scales;   // fp16 [N][K/G]
     const uint8_t *zeros;     // uint8 [N][K/G] or nullptr (then zero_const)
@@ -35,6 +35,7 @@ struct DecodeParams {
     int *status;              // device status word
     long long row_bytes;      // K * b / 8
     int M, N, K, group_log2, y_bf16;
+    int x_bf16;               // activations are bf16 (converted to fp16 as they are staged)
     int zero_const;           // the zero of every group when zeros == nullptr
     int vec_sz;               // scales 16-byte and zeros 8-byte aligned: vector staging
     DecodePlan pl;

@@ -101,29 +101,34 @@ QMM_API qmm_status qmm_unpack(const uint8_t *packed, uint8_t *codes, int N, int 
 
 /* Decode / skinny matmul, 1 <= M <= 16 (BitLLM sec. 5.1 decodes at batch 1;
  * the skinny range covers small batches).  Streams the bitstream through
- * shared memory with TMA, extracts codes in registers and accumulates in
- * fp32 on tensor cores.
- *   x        (device) [M][K] activations, dtype x_dtype (QMM_F16 only).
+ * shared memory with bulk copies (TMA), extracts codes in registers and
+ * accumulates in fp32 on tensor cores.
+ *   x        (device) [M][K] activations, dtype x_dtype: QMM_F16, or QMM_BF16
+ *            where the decode kernel takes the shape (see below; bf16 values
+ *            are converted to fp16 as they are staged, exactly for magnitudes
+ *            in [2^-14, 65504], to the fp16 subnormal grid below; magnitudes
+ *            above 65504 are outside the contract).  16-byte aligned.
  *   packed   (device) [N][K*bits/8] bitstream, 16-byte aligned.
  *   bits     1..8.   group: G in {32, 64, 128}, K % G == 0.
  *   scales   (device) fp16 [N][K/G].
  *   zeros    (device) uint8 [N][K/G], or NULL to use zero_const for every
  *            group (0 <= zero_const <= 255).
  *   y        (device) [M][N], dtype y_dtype (QMM_F16 or QMM_BF16).
- * The tensor cores see the integer codes q exactly (as fp16) and the fp16
- * activations, and accumulate each group in fp32; the group's scale and zero
- * are applied in fp32 afterwards as s*(sum q*x - z*sum x), which equals
- * sum s*(q - z)*x.  Results are deterministic run to run.
- * Two kernels serve the call.  The decode kernel takes M <= 8, G in {64, 128},
- * K % (8*G) == 0, N <= 32 x the SM count and a 16-byte aligned `packed`: each
- * warp reads its share of K
- * straight from global memory into the MMA operands, with no shared-memory
- * staging.  The skinny kernel takes every other shape: it stages the
- * activations in shared memory, and M x K fp16 must fit there next to the
- * weight pipeline (M*K <= 64K elements for M <= 8 and K = 4096 class shapes;
- * larger return QMM_ERR_UNSUPPORTED).  The two sum in different orders, so
- * their outputs may differ in the last bits.  qmm_set_gemv_kernel() forces the
- * skinny kernel.  K % 32 == 0 is implied by the group rule. */
+ * The tensor cores see the integer codes q exactly (as fp16 2^E + q) and the
+ * fp16 activations, and accumulate each group in fp32; the group's offset,
+ * scale and zero are applied in fp32 afterwards as s*(sum (2^E+q)*x - sum 2^E*x
+ * - z*sum x), which equals sum s*(q - z)*x.  Results are deterministic run to
+ * run.
+ * Two kernels serve the call (qmm_gemv_route() tells which).  The decode kernel
+ * takes G in {64, 128}, K % (8*G) == 0 and a 16-byte aligned `packed` when its
+ * planner finds a shared-memory layout: each CTA bulk-copies its weight rows
+ * into shared memory before waiting on the preceding kernel, then stages the
+ * activations.  The skinny kernel takes every other shape (fp16 activations
+ * only: QMM_BF16 there returns QMM_ERR_UNSUPPORTED); M x K fp16 must fit in
+ * its shared memory next to the weight pipeline (larger return
+ * QMM_ERR_UNSUPPORTED).  The two sum in different orders, so their outputs may
+ * differ in the last bits.  qmm_set_gemv_kernel() forces the skinny kernel.
+ * K % 32 == 0 is implied by the group rule. */
 QMM_API qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int bits,
                     int group, const void *scales, const uint8_t *zeros, int zero_const,
                     void *y, qmm_dtype y_dtype, int M, int N, int K, cudaStream_t stream);
