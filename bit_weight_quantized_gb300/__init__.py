@@ -144,7 +144,8 @@ def qmm_unpack(packed: torch.Tensor, K: int, bits: int) -> torch.Tensor:
     return out
 
 
-def _qmm(name, x, packed, bits, group, scales, zeros, zero_const, out, out_dtype):
+def _qmm_checks(x, packed, bits, group, scales, zeros, out, out_dtype):
+    # the argument checks one by one, for a precise error message
     _dev(x, "x")
     M, K = x.shape
     _dev(packed, "packed", torch.uint8)
@@ -156,13 +157,34 @@ def _qmm(name, x, packed, bits, group, scales, zeros, zero_const, out, out_dtype
         _dev(zeros, "zeros", torch.uint8, (N, K // group))
     if x.dtype not in _DT:
         raise ValueError("x must be float16 or bfloat16")
+    _dev(out, "out", out_dtype, (M, N))
+
+
+_U8, _F16 = torch.uint8, torch.float16
+
+
+def _qmm(name, x, packed, bits, group, scales, zeros, zero_const, out, out_dtype):
+    # the common path of the gemv/gemm calls, with the checks folded into one
+    # expression (a call costs a few microseconds of host time; the checks were
+    # a third of it); any failure re-runs them one by one for the message
+    xdt = x.dtype
+    M, K = x.shape
+    N = packed.shape[0]
     if out_dtype is None:
-        out_dtype = out.dtype if out is not None else x.dtype
+        out_dtype = out.dtype if out is not None else xdt
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=x.device)
-    _dev(out, "out", out_dtype, (M, N))
+    ng = K // group
+    if not (x.is_cuda and x.is_contiguous() and xdt in _DT and packed.is_cuda and packed.is_contiguous()
+            and packed.dtype is _U8 and packed.shape[1] * 8 == K * bits and scales.is_cuda
+            and scales.is_contiguous() and scales.dtype is _F16 and scales.shape == (N, ng) and out.is_cuda
+            and out.is_contiguous() and out.dtype is out_dtype and out.shape == (M, N)
+            and (zeros is None or (zeros.is_cuda and zeros.is_contiguous() and zeros.dtype is _U8
+                                   and zeros.shape == (N, ng)))):
+        _qmm_checks(x, packed, bits, group, scales, zeros, out, out_dtype)
+        raise ValueError(f"{name}: arguments do not match")
     fn = _FN.get(name) or getattr(load(), name)
-    st = fn(x.data_ptr(), _DT[x.dtype], packed.data_ptr(), bits, group, scales.data_ptr(),
+    st = fn(x.data_ptr(), _DT[xdt], packed.data_ptr(), bits, group, scales.data_ptr(),
             None if zeros is None else zeros.data_ptr(), int(zero_const), out.data_ptr(),
             _DT[out_dtype], M, N, K, _stream(x.get_device()))
     if st:
