@@ -495,24 +495,37 @@ def run_ours(args, world, rank, local):
     with torch.cuda.graph(gA, stream=stream):
         for c in range(copies):
             step(c)
-    reps = max(1, args.steps // copies)
-    steps = reps * copies
+    # exactly args.steps steps: whole replays of graph A, then a graph of the
+    # remaining steps (copies 0 .. rem - 1)
+    reps, rem = divmod(args.steps, copies)
+    steps = args.steps
+    gR = None
+    if rem:
+        gR = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gR, stream=stream):
+            for c in range(rem):
+                step(c)
     warm_reps = max(1, -(-args.warmup // copies))
-    for _ in range(warm_reps):
-        gA.replay()
-    torch.cuda.synchronize()
 
     clocks = ClockSampler(local)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     clocks.start()
     time.sleep(0.3)
+    # the warm-up steps right before the timed region (after the clock
+    # sampler's start-up pause, so the timed steps do not begin on an idle GPU)
+    with torch.cuda.stream(stream):
+        for _ in range(warm_reps):
+            gA.replay()
+    torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(reps):
             gA.replay()
+        if gR is not None:
+            gR.replay()
         e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
