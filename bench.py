@@ -426,6 +426,17 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf, gemv_kernel="auto",
     out["float6_e3m2_M1"] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
                              "frac_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4)}
     del fsets
+    # 4- and 8-bit float codes (e2m1, e4m3), M = 1, K = N = 4096, group 128: the
+    # decode kernel's tensor-core path
+    for (e, m) in ((2, 1), (4, 3)):
+        b = 1 + e + m
+        fsets = [(q.qmm_pack(codes(N, K, b), b), scales(N, K // 128)) for _ in range(ncopies(N * K * b // 8))]
+        ms = time_graph(torch, stream, [lambda w=w_, e=e, m=m: q.qmm_gemv_float(x, w[0], e, m, 128, w[1], out=y)
+                                        for w_ in fsets])
+        nbytes = N * K * b // 8 + N * (K // 128) * 2 + K * 2 + N * 2
+        out[f"float{b}_e{e}m{m}_M1"] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
+                                        "frac_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4)}
+    del fsets
     # per-token int8 activation quantizer alone: K = 4096, inputs rotate over 8 copies
     K = 4096
     for M in (1, 64, 2048):

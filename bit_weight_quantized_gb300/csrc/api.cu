@@ -255,6 +255,33 @@ qmm_status qmm_gemv_float(const void *x, const uint8_t *packed, int ebits, int m
         return QMM_ERR_DEVICE;
     if (K == 0)
         return from_cuda(cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * 2, stream));
+    // 4- and 8-bit codes with at most 4 exponent bits are exact fp16 numbers
+    // (times a power of two; a 5-bit exponent field of 31 would read as inf):
+    // the decode kernel runs them on the tensor cores
+    const int bits = 1 + ebits + mbits;
+    DecodePlan plan;
+    if ((bits == 4 || bits == 8) && ebits <= 4 && aligned(packed, 16) &&
+        decode_plan(M, N, K, group, bits, false, false, f->num_sms, f->smem_pair, f->smem_optin, &plan)) {
+        DecodeParams d;
+        std::memset(&d, 0, sizeof(d));
+        d.x = static_cast<const uint16_t *>(x);
+        d.packed = packed;
+        d.scales = static_cast<const uint16_t *>(scales);
+        d.zeros = nullptr;
+        d.y = y;
+        d.status = f->status;
+        d.row_bytes = static_cast<long long>(K) * bits / 8;
+        d.M = M;
+        d.N = N;
+        d.K = K;
+        d.group_log2 = group == 64 ? 6 : 7;
+        d.zero_const = 0;
+        d.ebits = ebits;
+        d.mbits = mbits;
+        d.fscale = static_cast<float>(1 << (15 - ((1 << (ebits - 1)) - 1)));
+        d.pl = plan;
+        return from_cuda(launch_decode_float(d, bits, stream));
+    }
     return from_cuda(launch_gemv_fp(static_cast<const uint16_t *>(x), packed, ebits, mbits, group,
                                     static_cast<const uint16_t *>(scales), static_cast<uint16_t *>(y), M, N,
                                     K, stream));

@@ -158,9 +158,37 @@ __device__ __forceinline__ void issue_chunk(const DecodeParams &p, uint8_t *slot
 // SM) MMAs j = 0, 2 and j = 1, 3 go to separate accumulator sets (summed at
 // the fold), which halves the dependent chains; with one (two CTAs per SM, 128
 // registers) a single set measured faster.
-template <int B, int NT>
+// Float codes (sign, e exponent bits, m mantissa bits; b = 4 or 8, e <= 4) of
+// the 16-code run in w, as fp16 pairs in code order (pair q = codes 2q, 2q + 1):
+// the exponent and mantissa fields go to the top of the fp16 exponent and
+// mantissa fields and the sign to bit 15, which reads exactly the code's value
+// times 2^(bias - 15) (normal and subnormal codes alike).  fl = {mask of the e + m
+// low bits in both halves, shift of that field, shift of the sign}.
+template <int B>
+__device__ __forceinline__ void extract_float_run(const uint32_t (&w)[run_words<B>()], uint3 fl, uint32_t (&a)[8])
+{
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        uint32_t t;
+        if constexpr (B == 4) {   // nibbles 2j, 2j + 1 of word q / 4 to the low nibble of each half
+            const uint32_t wq = w[q >> 2];
+            const uint32_t j = static_cast<uint32_t>(q & 3);
+            t = prmt(wq, wq >> 4, j | ((4u + j) << 8));
+        } else {                  // bytes 2q, 2q + 1 to the low byte of each half
+            const uint32_t b0 = static_cast<uint32_t>(2 * (q & 1));
+            t = prmt(w[q >> 1], 0u, b0 | (4u << 4) | ((b0 + 1u) << 8) | (4u << 12));
+        }
+        uint32_t r;
+        asm("lop3.b32 %0, %1, %2, %3, 0xF8;"   // a | (b & c)
+            : "=r"(r)
+            : "r"((t & fl.x) << fl.y), "r"(t << fl.z), "r"(0x80008000u));
+        a[q] = r;
+    }
+}
+
+template <int B, int NT, bool FL>
 __device__ __forceinline__ void block_mma(const uint8_t *const (&run0)[2][2], int boff, const uint8_t *xb,
-                                          int x_pitch, int m0, int m1, int o, float (&acc)[2][2][NT][4])
+                                          int x_pitch, int m0, int m1, int o, uint3 fl, float (&acc)[2][2][NT][4])
 {
     constexpr int NW = run_words<B>();
     uint32_t a[2][2][8];
@@ -170,7 +198,10 @@ __device__ __forceinline__ void block_mma(const uint8_t *const (&run0)[2][2], in
         for (int h = 0; h < 2; ++h) {
             uint32_t w[NW];
             load_run<B>(w, run0[i][h] + boff, o);
-            extract_run<B, 16, false, false>(w, a[i][h]);
+            if constexpr (FL)
+                extract_float_run<B>(w, fl, a[i][h]);
+            else
+                extract_run<B, 16, false, false>(w, a[i][h]);
         }
     uint32_t xw[NT][8];
 #pragma unroll
@@ -196,7 +227,7 @@ __device__ __forceinline__ void block_mma(const uint8_t *const (&run0)[2][2], in
 // order) in fragment (slot) order: slot s of the run holds x of the run's code
 // code_of_slot(s).  Returns the run's sums X = sum x and C = sum 2^E x (E of
 // each code's position in the plan), in fp32.
-template <int B>
+template <int B, bool FL>
 __device__ __forceinline__ float2 stage_run(uint8_t *dst, const uint4 (&raw)[2], bool x_bf16)
 {
     uint32_t in[8] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w};
@@ -215,7 +246,8 @@ __device__ __forceinline__ float2 stage_run(uint8_t *dst, const uint4 (&raw)[2],
     uint32_t out[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-        const int c1 = code_of_slot<B, 16>(2 * q), c2 = code_of_slot<B, 16>(2 * q + 1);
+        // float codes pair in code order (slot s = code s)
+        const int c1 = FL ? 2 * q : code_of_slot<B, 16>(2 * q), c2 = FL ? 2 * q + 1 : code_of_slot<B, 16>(2 * q + 1);
         out[q] = prmt(in[c1 >> 1], in[c2 >> 1], half_sel(c1 & 1, c2 & 1));
     }
     *reinterpret_cast<uint4 *>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
@@ -225,14 +257,15 @@ __device__ __forceinline__ float2 stage_run(uint8_t *dst, const uint4 (&raw)[2],
     for (int c = 0; c < 16; ++c) {
         const float v = f16_bits_to_f32(static_cast<uint16_t>(in[c >> 1] >> (16 * (c & 1))));
         X += v;
-        C = fmaf(static_cast<float>(1 << exp_of_code<B, 16>(c)), v, C);
+        if constexpr (!FL)   // float codes carry no offset
+            C = fmaf(static_cast<float>(1 << exp_of_code<B, 16>(c)), v, C);
     }
     return make_float2(X, C);
 }
 
 // The activation staging of more than one round (several tokens or long K),
 // kept out of line so that the one-round path of the decode shapes stays compact.
-template <int B, int NB>
+template <int B, int NB, bool FL>
 __device__ __noinline__ void stage_rounds(const DecodeParams &p, uint8_t *xw, float2 *xs, int warp, int lane,
                                           int rounds)
 {
@@ -268,7 +301,7 @@ __device__ __noinline__ void stage_rounds(const DecodeParams &p, uint8_t *xw, fl
                     break;
                 float2 v = make_float2(0.f, 0.f);
                 if (jq[q] < pl.nseg)
-                    v = stage_run<B>(xw + mq[q] * pl.x_pitch + ((jq[q] * NB + bb) * 64 + 16 * tq) * 2, raw[q],
+                    v = stage_run<B, FL>(xw + mq[q] * pl.x_pitch + ((jq[q] * NB + bb) * 64 + 16 * tq) * 2, raw[q],
                                      p.x_bf16 != 0);
 #pragma unroll
                 for (int off = 1; off < 4 * NB; off <<= 1) {
@@ -283,7 +316,7 @@ __device__ __noinline__ void stage_rounds(const DecodeParams &p, uint8_t *xw, fl
 
 // NB = G / 64 blocks per group; warp w owns group w of every 8-group segment.
 // TILE: the weights are in the fragment-ordered (tile16) layout.
-template <int B, int NT, int NB, bool TILE>
+template <int B, int NT, int NB, bool TILE, bool FL>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
 decode_kernel(const DecodeParams p)
 {
@@ -402,7 +435,7 @@ decode_kernel(const DecodeParams p)
                 const uint16_t *src = p.x + jl * pl.kseg + 64 * (warp * NB + bb) + 16 * tq;
                 const uint4 raw[2] = {*reinterpret_cast<const uint4 *>(src),
                                       *reinterpret_cast<const uint4 *>(src + 8)};
-                v = stage_run<B>(xw + ((jl * NB + bb) * 64 + 16 * tq) * 2, raw, p.x_bf16 != 0);
+                v = stage_run<B, FL>(xw + ((jl * NB + bb) * 64 + 16 * tq) * 2, raw, p.x_bf16 != 0);
             }
 #pragma unroll
             for (int off = 1; off < 4 * NB; off <<= 1) {
@@ -413,7 +446,7 @@ decode_kernel(const DecodeParams p)
                 xs[jl] = v;
         }
         if (rounds > 1)
-            stage_rounds<B, NB>(p, xw, xs, warp, lane, rounds);
+            stage_rounds<B, NB, FL>(p, xw, xs, warp, lane, rounds);
         __syncwarp();
     }
 
@@ -422,6 +455,8 @@ decode_kernel(const DecodeParams p)
     const int first_b = (16 * B * t) / 32 * 4;          // byte of the thread's first word in a block
     const int o = (B & 1) ? 16 * (t & 1) : 0;           // bit offset of its run in that word
     const float zc = p.zeros ? 0.f : static_cast<float>(p.zero_const);
+    const uint3 fl = make_uint3(((1u << (p.ebits + p.mbits)) - 1u) * 0x00010001u, static_cast<uint32_t>(10 - p.mbits),
+                                static_cast<uint32_t>(15 - p.ebits - p.mbits));
     bool ok = true;
     int slot = 0;
     uint32_t par = 0;
@@ -482,8 +517,9 @@ decode_kernel(const DecodeParams p)
                         // block kblock of the chunk: 8 b bytes apart per row (canonical), or one
                         // 16-row unit of 128 b bytes apart (tile16)
                         const int kblock = jj * (pl.kseg / 64) + warp * NB + bb;
-                        block_mma<B, NT>(run0, kblock * (TILE ? 128 * B : 8 * B),
-                                         xw + ((j * NB + bb) * 64 + 16 * t) * 2, pl.x_pitch, m0, m1, o, acc);
+                        block_mma<B, NT, FL>(run0, kblock * (TILE ? 128 * B : 8 * B),
+                                             xw + ((j * NB + bb) * 64 + 16 * t) * 2, pl.x_pitch, m0, m1, o, fl,
+                                             acc);
                     }
                     // the group's offset, zero and scale: tot += s (acc - C - z X)
                     const int gidx = j * kWarps + warp;
@@ -502,7 +538,7 @@ decode_kernel(const DecodeParams p)
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             const int e = gidx * nrows + rr + lr[i][h];
-                            const float s = f16_bits_to_f32(sc[e]);
+                            const float s = FL ? f16_bits_to_f32(sc[e]) * p.fscale : f16_bits_to_f32(sc[e]);
                             const float z = p.zeros ? f16_bits_to_f32(zo[e]) : 0.f;
 #pragma unroll
                             for (int tt = 0; tt < NT; ++tt)
@@ -573,10 +609,10 @@ decode_kernel(const DecodeParams p)
     }
 }
 
-template <int B, int NT, int NB, bool TILE>
+template <int B, int NT, int NB, bool TILE, bool FL>
 cudaError_t launch_decode_b(const DecodeParams &p, cudaStream_t stream)
 {
-    auto kern = decode_kernel<B, NT, NB, TILE>;
+    auto kern = decode_kernel<B, NT, NB, TILE, FL>;
     static SmemLimit limit;
     if (const cudaError_t e = ensure_smem_limit(limit, kern, p.pl.smem, true); e != cudaSuccess)
         return e;
@@ -597,14 +633,14 @@ template <int NT, int NB, bool TILE>
 cudaError_t launch_decode_cfg(const DecodeParams &p, int bits, cudaStream_t stream)
 {
     switch (bits) {
-    case 1: return launch_decode_b<1, NT, NB, TILE>(p, stream);
-    case 2: return launch_decode_b<2, NT, NB, TILE>(p, stream);
-    case 3: return launch_decode_b<3, NT, NB, TILE>(p, stream);
-    case 4: return launch_decode_b<4, NT, NB, TILE>(p, stream);
-    case 5: return launch_decode_b<5, NT, NB, TILE>(p, stream);
-    case 6: return launch_decode_b<6, NT, NB, TILE>(p, stream);
-    case 7: return launch_decode_b<7, NT, NB, TILE>(p, stream);
-    case 8: return launch_decode_b<8, NT, NB, TILE>(p, stream);
+    case 1: return launch_decode_b<1, NT, NB, TILE, false>(p, stream);
+    case 2: return launch_decode_b<2, NT, NB, TILE, false>(p, stream);
+    case 3: return launch_decode_b<3, NT, NB, TILE, false>(p, stream);
+    case 4: return launch_decode_b<4, NT, NB, TILE, false>(p, stream);
+    case 5: return launch_decode_b<5, NT, NB, TILE, false>(p, stream);
+    case 6: return launch_decode_b<6, NT, NB, TILE, false>(p, stream);
+    case 7: return launch_decode_b<7, NT, NB, TILE, false>(p, stream);
+    case 8: return launch_decode_b<8, NT, NB, TILE, false>(p, stream);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -617,6 +653,21 @@ cudaError_t launch_decode_layout(const DecodeParams &p, int bits, cudaStream_t s
     if (p.M > 8)
         return g128 ? launch_decode_cfg<2, 2, TILE>(p, bits, stream) : launch_decode_cfg<2, 1, TILE>(p, bits, stream);
     return g128 ? launch_decode_cfg<1, 2, TILE>(p, bits, stream) : launch_decode_cfg<1, 1, TILE>(p, bits, stream);
+}
+
+// Float codes of 4 or 8 bits (canonical layout).
+template <int NT, int NB>
+cudaError_t launch_decode_float_cfg(const DecodeParams &p, int bits, cudaStream_t stream)
+{
+    return bits == 4 ? launch_decode_b<4, NT, NB, false, true>(p, stream) : launch_decode_b<8, NT, NB, false, true>(p, stream);
+}
+
+inline cudaError_t launch_decode_float_layout(const DecodeParams &p, int bits, cudaStream_t stream)
+{
+    const bool g128 = p.group_log2 == 7;
+    if (p.M > 8)
+        return g128 ? launch_decode_float_cfg<2, 2>(p, bits, stream) : launch_decode_float_cfg<2, 1>(p, bits, stream);
+    return g128 ? launch_decode_float_cfg<1, 2>(p, bits, stream) : launch_decode_float_cfg<1, 1>(p, bits, stream);
 }
 
 }  // namespace

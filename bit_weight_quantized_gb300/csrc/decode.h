@@ -38,6 +38,8 @@ struct DecodeParams {
     int x_bf16;               // activations are bf16 (converted to fp16 as they are staged)
     int zero_const;           // the zero of every group when zeros == nullptr
     int vec_sz;               // scales 16-byte and zeros 8-byte aligned: vector staging
+    int ebits, mbits;         // float codes: exponent and mantissa bits (0 for integer codes)
+    float fscale;             // float codes: 2^(15 - bias), folded into the scale
     DecodePlan pl;
 };
 
@@ -51,5 +53,7 @@ bool decode_plan(int M, int N, int K, int group, int bits, bool stored_zeros, bo
 // tile16: the weights are in the fragment-ordered layout (qmm_repack).
 cudaError_t launch_decode(const DecodeParams &p, int bits, bool tile16, cudaStream_t stream);
 cudaError_t launch_decode_tile16(const DecodeParams &p, int bits, cudaStream_t stream);
+// Float codes (qmm_gemv_float): bits 4 or 8, at most 4 exponent bits.
+cudaError_t launch_decode_float(const DecodeParams &p, int bits, cudaStream_t stream);
 
 }  // namespace qmm

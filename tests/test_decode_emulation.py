@@ -387,3 +387,46 @@ def test_staged_kernel_emulation_small_ring(tmp_path):
     y = _emulate_staged(prob, oracle.pack(prob.codes, 8)[0], plan)
     ref = oracle.solve_qmm(prob)
     np.testing.assert_allclose(y, ref, rtol=0, atol=1e-9 * np.abs(ref).max())
+
+
+def _float_pair_bits(word, q, b, e, m):
+    """Emulates the decode kernel's float extraction of pair q of a 32-bit word
+    (b = 4: nibbles 2j, 2j + 1 of the word, j = q % 4; b = 8: bytes 2(q % 2),
+    2(q % 2) + 1): byte permute, masked field shifted to the top of the fp16
+    exponent/mantissa fields, sign to bit 15 of each half."""
+    def prmt(a, bb, sel):
+        src = [(a >> (8 * i)) & 0xFF for i in range(4)] + [(bb >> (8 * i)) & 0xFF for i in range(4)]
+        return sum(src[(sel >> (4 * k)) & 7] << (8 * k) for k in range(4))
+    if b == 4:
+        j = q & 3
+        t = prmt(word, word >> 4, j | ((4 + j) << 8))
+    else:
+        b0 = 2 * (q & 1)
+        t = prmt(word, 0, b0 | (4 << 4) | ((b0 + 1) << 8) | (4 << 12))
+    mask = ((1 << (e + m)) - 1) * 0x00010001
+    em = ((t & mask) << (10 - m)) & 0xFFFFFFFF
+    sg = (t << (15 - e - m)) & 0x80008000
+    return em | sg
+
+
+@pytest.mark.parametrize("b,e", [(4, 1), (4, 2), (4, 3), (8, 1), (8, 2), (8, 3), (8, 4)])
+def test_float_code_extraction_is_exact(b, e):
+    # every code of the split through the extraction: fp16 value = code value * 2^(bias - 15).
+    # (e = 5 is left to the FFMA kernel: its top exponent field would read as inf in fp16)
+    import oracle
+    m = b - 1 - e
+    bias = (1 << (e - 1)) - 1
+    for q in range(8 if b == 4 else 2):
+        for c in range(1 << b):
+            for c2 in (0, (1 << b) - 1, c ^ 1):
+                if b == 4:   # code c at nibble 2j, c2 at 2j + 1 of a word, other nibbles noise
+                    j = q & 3
+                    word = 0x9A5C3E71 & ~(0xFF << (8 * j)) | (c << (8 * j)) | (c2 << (8 * j + 4))
+                else:        # code c at byte 2(q % 2), c2 at the next byte
+                    b0 = 2 * (q & 1)
+                    word = 0xB4D27E19 & ~(0xFFFF << (8 * b0)) | (c << (8 * b0)) | (c2 << (8 * b0 + 8))
+                bits = _float_pair_bits(word, q, b, e, m)
+                lo = np.array([bits & 0xFFFF], dtype=np.uint16).view(np.float16)[0]
+                hi = np.array([bits >> 16], dtype=np.uint16).view(np.float16)[0]
+                assert float(lo) == oracle.float_value(c, e, m) * 2.0 ** (bias - 15)
+                assert float(hi) == oracle.float_value(c2, e, m) * 2.0 ** (bias - 15)

@@ -49,3 +49,18 @@ def test_float_weights_parity(q, e, m):
 def test_float6_e3m2_shapes(q, M, N, K, G):
     y, ref = run_case(q, 3, 2, M, N, K, G, seed=M + N)
     assert rel_err(y, ref) <= REL_TOL
+
+
+@pytest.mark.parametrize("e,m", [(2, 1), (1, 2), (3, 0), (4, 3), (3, 4), (2, 5)])
+@pytest.mark.parametrize("M", [1, 16])
+def test_float4_float8_decode_shapes(q, e, m, M):
+    # 4- and 8-bit float codes (at most 4 exponent bits) run on the decode
+    # kernel's tensor-core path: the decode sweep shape, group 128
+    y, ref = run_case(q, e, m, M, 4096, 4096, 128, seed=e * 100 + m * 10 + M)
+    assert rel_err(y, ref) <= REL_TOL
+
+
+@pytest.mark.parametrize("e,m", [(2, 1), (4, 3)])
+def test_float_decode_group64_ragged(q, e, m):
+    y, ref = run_case(q, e, m, 9, 333, 1024, 64, seed=e + m)
+    assert rel_err(y, ref) <= REL_TOL
