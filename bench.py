@@ -417,7 +417,8 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf, gemv_kernel="auto",
                                  "frac_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4),
                                  "TOPs": round(2.0 * M * N * K / ms / 1e9, 1)}
     del wsets
-    # float weights: float6 e3m2 (FP6-like), M = 1, K = N = 4096, group 128
+    # float weights on the decode kernel's tensor-core path: float6 e3m2
+    # (FP6-like), M = 1, K = N = 4096, group 128
     fsets = [(q.qmm_pack(codes(N, K, 6), 6), scales(N, K // 128)) for _ in range(ncopies(N * K * 6 // 8))]
     x = torch.randn(1, K, device=dev, generator=gen).half()
     y = torch.empty(1, N, dtype=torch.float16, device=dev)
@@ -426,8 +427,7 @@ def measure_others(torch, q, dev, stream, peak_gbs, peak_tf, gemv_kernel="auto",
     out["float6_e3m2_M1"] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
                              "frac_hbm": round(nbytes / ms / 1e6 / peak_gbs, 4)}
     del fsets
-    # 4- and 8-bit float codes (e2m1, e4m3), M = 1, K = N = 4096, group 128: the
-    # decode kernel's tensor-core path
+    # 4- and 8-bit float codes (e2m1, e4m3), the same shape
     for (e, m) in ((2, 1), (4, 3)):
         b = 1 + e + m
         fsets = [(q.qmm_pack(codes(N, K, b), b), scales(N, K // 128)) for _ in range(ncopies(N * K * b // 8))]

@@ -255,12 +255,12 @@ qmm_status qmm_gemv_float(const void *x, const uint8_t *packed, int ebits, int m
         return QMM_ERR_DEVICE;
     if (K == 0)
         return from_cuda(cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * 2, stream));
-    // 4- and 8-bit codes with at most 4 exponent bits are exact fp16 numbers
-    // (times a power of two; a 5-bit exponent field of 31 would read as inf):
-    // the decode kernel runs them on the tensor cores
+    // codes with at most 4 exponent bits are exact fp16 numbers (times a power
+    // of two; a 5-bit exponent field of 31 would read as inf): the decode
+    // kernel runs them on the tensor cores
     const int bits = 1 + ebits + mbits;
     DecodePlan plan;
-    if ((bits == 4 || bits == 8) && ebits <= 4 && aligned(packed, 16) &&
+    if (ebits <= 4 && aligned(packed, 16) &&
         decode_plan(M, N, K, group, bits, false, false, f->num_sms, f->smem_pair, f->smem_optin, &plan)) {
         DecodeParams d;
         std::memset(&d, 0, sizeof(d));

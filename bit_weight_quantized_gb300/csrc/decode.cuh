@@ -158,12 +158,24 @@ __device__ __forceinline__ void issue_chunk(const DecodeParams &p, uint8_t *slot
 // SM) MMAs j = 0, 2 and j = 1, 3 go to separate accumulator sets (summed at
 // the fold), which halves the dependent chains; with one (two CTAs per SM, 128
 // registers) a single set measured faster.
-// Float codes (sign, e exponent bits, m mantissa bits; b = 4 or 8, e <= 4) of
-// the 16-code run in w, as fp16 pairs in code order (pair q = codes 2q, 2q + 1):
-// the exponent and mantissa fields go to the top of the fp16 exponent and
-// mantissa fields and the sign to bit 15, which reads exactly the code's value
-// times 2^(bias - 15) (normal and subnormal codes alike).  fl = {mask of the e + m
-// low bits in both halves, shift of that field, shift of the sign}.
+// Code k of a run whose code 0 sits at bit 0 of w[0], at bit 0 of the result
+// (higher bits hold the following codes).
+template <int B>
+__device__ __forceinline__ uint32_t run_code_at0(const uint32_t (&w)[run_words<B>()], int k)
+{
+    constexpr int NW = run_words<B>();
+    const int bit = B * k, i = bit >> 5, sh = bit & 31;
+    if (sh == 0)
+        return w[i];
+    return i + 1 < NW ? __funnelshift_r(w[i], w[i + 1], sh) : w[i] >> sh;
+}
+
+// Float codes (sign, e exponent bits, m mantissa bits; e <= 4) of the 16-code
+// run in w, as fp16 pairs in code order (pair q = codes 2q, 2q + 1): the
+// exponent and mantissa fields go to the top of the fp16 exponent and mantissa
+// fields and the sign to bit 15, which reads exactly the code's value times
+// 2^(bias - 15) (normal and subnormal codes alike).  fl = {mask of the e + m low
+// bits in both halves, shift of that field, shift of the sign}.
 template <int B>
 __device__ __forceinline__ void extract_float_run(const uint32_t (&w)[run_words<B>()], uint3 fl, uint32_t (&a)[8])
 {
@@ -174,9 +186,11 @@ __device__ __forceinline__ void extract_float_run(const uint32_t (&w)[run_words<
             const uint32_t wq = w[q >> 2];
             const uint32_t j = static_cast<uint32_t>(q & 3);
             t = prmt(wq, wq >> 4, j | ((4u + j) << 8));
-        } else {                  // bytes 2q, 2q + 1 to the low byte of each half
+        } else if constexpr (B == 8) {   // bytes 2q, 2q + 1 to the low byte of each half
             const uint32_t b0 = static_cast<uint32_t>(2 * (q & 1));
             t = prmt(w[q >> 1], 0u, b0 | (4u << 4) | ((b0 + 1u) << 8) | (4u << 12));
+        } else {   // other widths: each code of the pair shifted to bit 0, low halves joined
+            t = prmt(run_code_at0<B>(w, 2 * q), run_code_at0<B>(w, 2 * q + 1), 0x5410u);
         }
         uint32_t r;
         asm("lop3.b32 %0, %1, %2, %3, 0xF8;"   // a | (b & c)
@@ -655,19 +669,14 @@ cudaError_t launch_decode_layout(const DecodeParams &p, int bits, cudaStream_t s
     return g128 ? launch_decode_cfg<1, 2, TILE>(p, bits, stream) : launch_decode_cfg<1, 1, TILE>(p, bits, stream);
 }
 
-// Float codes of 4 or 8 bits (canonical layout).
-template <int NT, int NB>
-cudaError_t launch_decode_float_cfg(const DecodeParams &p, int bits, cudaStream_t stream)
-{
-    return bits == 4 ? launch_decode_b<4, NT, NB, false, true>(p, stream) : launch_decode_b<8, NT, NB, false, true>(p, stream);
-}
-
-inline cudaError_t launch_decode_float_layout(const DecodeParams &p, int bits, cudaStream_t stream)
+// Float codes of width B (canonical layout), every configuration.
+template <int B>
+cudaError_t launch_decode_float_width(const DecodeParams &p, cudaStream_t stream)
 {
     const bool g128 = p.group_log2 == 7;
     if (p.M > 8)
-        return g128 ? launch_decode_float_cfg<2, 2>(p, bits, stream) : launch_decode_float_cfg<2, 1>(p, bits, stream);
-    return g128 ? launch_decode_float_cfg<1, 2>(p, bits, stream) : launch_decode_float_cfg<1, 1>(p, bits, stream);
+        return g128 ? launch_decode_b<B, 2, 2, false, true>(p, stream) : launch_decode_b<B, 2, 1, false, true>(p, stream);
+    return g128 ? launch_decode_b<B, 1, 2, false, true>(p, stream) : launch_decode_b<B, 1, 1, false, true>(p, stream);
 }
 
 }  // namespace

@@ -202,13 +202,13 @@ QMM_API qmm_status qmm_w4a8(const int8_t *xq, const void *sa, const uint8_t *w4,
  *   scales  (device) fp16 [N][K/G]; G in {32, 64, 128}, K % G == 0.
  *   y       (device) fp16 [M][N], fully overwritten (fp32 accumulation, RNE).
  * Products of a weight and an activation are exact in fp32; the sums round.
- * Two kernels serve it.  4- and 8-bit codes with ebits <= 4, G in {64, 128},
+ * Two kernels serve it.  Codes with ebits <= 4, G in {64, 128},
  * K % (8*G) == 0 and a 16-byte aligned `packed` run on the decode kernel's
  * tensor-core path: a code's exponent and mantissa fields placed at the top of
  * the fp16 fields and its sign at bit 15 read exactly as its value times
- * 2^(bias - 15), a power of two folded into the group scale.  Every other
- * split (and e5m2, whose top exponent would read as inf in fp16) runs on an
- * FFMA kernel.
+ * 2^(bias - 15), a power of two folded into the group scale.  Everything else
+ * (ebits = 5, whose top exponent would read as inf in fp16; G = 32; other
+ * shapes) runs on an FFMA kernel.
  * Errors: QMM_ERR_BITS (ebits < 1 or b outside 2..8), QMM_ERR_SHAPE,
  * QMM_ERR_NULL, QMM_ERR_ALIGN, QMM_ERR_DEVICE, QMM_ERR_CUDA. */
 QMM_API qmm_status qmm_gemv_float(const void *x, const uint8_t *packed, int ebits, int mbits,

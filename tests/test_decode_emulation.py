@@ -409,6 +409,40 @@ def _float_pair_bits(word, q, b, e, m):
     return em | sg
 
 
+def _float_pair_bits_any(run, q, b, e, m):
+    """The extraction at widths other than 4 and 8: run = the 16-code run as an
+    integer (code k at bit b k); codes 2q and 2q + 1 are each shifted to bit 0 of
+    a 32-bit word (the following codes above them) and the low halves joined,
+    then masked and shifted as at b = 4, 8."""
+    nbits = 32 * ((b + 1) // 2)
+    def at0(k):
+        return (run >> (b * k)) & 0xFFFFFFFF if b * k < nbits else 0
+    t = (at0(2 * q) & 0xFFFF) | ((at0(2 * q + 1) & 0xFFFF) << 16)
+    mask = ((1 << (e + m)) - 1) * 0x00010001
+    em = ((t & mask) << (10 - m)) & 0xFFFFFFFF
+    sg = (t << (15 - e - m)) & 0x80008000
+    return em | sg
+
+
+@pytest.mark.parametrize("b,e", [(2, 1), (3, 1), (3, 2), (5, 2), (5, 4), (6, 3), (7, 3), (7, 4)])
+def test_float_code_extraction_any_width_is_exact(b, e):
+    import oracle
+    m = b - 1 - e
+    bias = (1 << (e - 1)) - 1
+    st = np.random.default_rng(b * 10 + e)
+    for q in range(8):
+        for c in range(1 << b):
+            for c2 in (0, (1 << b) - 1, c ^ 1):
+                codes = [int(v) for v in st.integers(0, 1 << b, 16)]
+                codes[2 * q], codes[2 * q + 1] = c, c2
+                run = sum(v << (b * k) for k, v in enumerate(codes))
+                bits = _float_pair_bits_any(run, q, b, e, m)
+                lo = np.array([bits & 0xFFFF], dtype=np.uint16).view(np.float16)[0]
+                hi = np.array([bits >> 16], dtype=np.uint16).view(np.float16)[0]
+                assert float(lo) == oracle.float_value(c, e, m) * 2.0 ** (bias - 15)
+                assert float(hi) == oracle.float_value(c2, e, m) * 2.0 ** (bias - 15)
+
+
 @pytest.mark.parametrize("b,e", [(4, 1), (4, 2), (4, 3), (8, 1), (8, 2), (8, 3), (8, 4)])
 def test_float_code_extraction_is_exact(b, e):
     # every code of the split through the extraction: fp16 value = code value * 2^(bias - 15).

@@ -51,16 +51,17 @@ def test_float6_e3m2_shapes(q, M, N, K, G):
     assert rel_err(y, ref) <= REL_TOL
 
 
-@pytest.mark.parametrize("e,m", [(2, 1), (1, 2), (3, 0), (4, 3), (3, 4), (2, 5)])
+@pytest.mark.parametrize("e,m", [(1, 0), (1, 1), (2, 0), (2, 1), (1, 2), (3, 0), (2, 2), (4, 0), (3, 2),
+                                 (2, 3), (3, 3), (4, 2), (4, 3), (3, 4), (2, 5)])
 @pytest.mark.parametrize("M", [1, 16])
-def test_float4_float8_decode_shapes(q, e, m, M):
-    # 4- and 8-bit float codes (at most 4 exponent bits) run on the decode
-    # kernel's tensor-core path: the decode sweep shape, group 128
+def test_float_decode_shapes(q, e, m, M):
+    # float codes of at most 4 exponent bits run on the decode kernel's
+    # tensor-core path: the decode sweep shape, group 128
     y, ref = run_case(q, e, m, M, 4096, 4096, 128, seed=e * 100 + m * 10 + M)
     assert rel_err(y, ref) <= REL_TOL
 
 
-@pytest.mark.parametrize("e,m", [(2, 1), (4, 3)])
+@pytest.mark.parametrize("e,m", [(1, 1), (2, 1), (2, 2), (3, 2), (3, 3), (4, 3)])
 def test_float_decode_group64_ragged(q, e, m):
     y, ref = run_case(q, e, m, 9, 333, 1024, 64, seed=e + m)
     assert rel_err(y, ref) <= REL_TOL
