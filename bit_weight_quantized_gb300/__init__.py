@@ -14,7 +14,9 @@ zeros are uint8 ``[N][K/G]`` or a constant.
 from __future__ import annotations
 
 import ctypes
+import importlib.util
 import os
+import sysconfig
 from typing import Optional
 
 import torch
@@ -57,6 +59,30 @@ SIGNATURES = {
 _lib = None
 _FN = {}   # name -> the configured ctypes function, filled by load()
 
+# The optional CPython fast-call extension (csrc/pyfast.c, built next to the
+# library): it calls the 14-argument entry points through their addresses,
+# without ctypes' per-argument conversion.  Without it the calls go through
+# ctypes; either way the same library function runs.
+FAST_PATH = os.path.join(_HERE, "lib", "_qmmfast" + (sysconfig.get_config_var("EXT_SUFFIX") or ".so"))
+_FAST_NAMES = ("qmm_gemv", "qmm_gemm", "qmm_gemv_tile16")
+_call14 = None
+_ADDR = {}   # name -> function address for _call14, filled by load()
+
+
+def _load_fastcall(lib):
+    global _call14
+    if not os.path.exists(FAST_PATH):
+        return
+    try:
+        spec = importlib.util.spec_from_file_location("_qmmfast", FAST_PATH)
+        mod = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(mod)
+    except (ImportError, OSError):
+        return
+    for name in _FAST_NAMES:
+        _ADDR[name] = ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+    _call14 = mod.call14
+
 
 class QmmError(RuntimeError):
     def __init__(self, status: int, where: str):
@@ -77,6 +103,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             fn.argtypes = args
             fn.restype = res
             _FN[name] = fn
+        _load_fastcall(lib)
         _lib = lib
     return _lib
 
@@ -183,10 +210,12 @@ def _qmm(name, x, packed, bits, group, scales, zeros, zero_const, out, out_dtype
                                    and zeros.shape == (N, ng)))):
         _qmm_checks(x, packed, bits, group, scales, zeros, out, out_dtype)
         raise ValueError(f"{name}: arguments do not match")
-    fn = _FN.get(name) or getattr(load(), name)
-    st = fn(x.data_ptr(), _DT[xdt], packed.data_ptr(), bits, group, scales.data_ptr(),
+    if _lib is None:
+        load()
+    args = (x.data_ptr(), _DT[xdt], packed.data_ptr(), bits, group, scales.data_ptr(),
             None if zeros is None else zeros.data_ptr(), int(zero_const), out.data_ptr(),
             _DT[out_dtype], M, N, K, _stream(x.get_device()))
+    st = _call14(_ADDR[name], *args) if _call14 is not None else _FN[name](*args)
     if st:
         raise QmmError(st, name)
     return out
@@ -239,10 +268,12 @@ def qmm_gemv_tile16(x, tiled, N, bits, group, scales, zeros=None, zero_const=0, 
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=x.device)
     _dev(out, "out", out_dtype, (M, N))
-    fn = _FN.get("qmm_gemv_tile16") or getattr(load(), "qmm_gemv_tile16")
-    st = fn(x.data_ptr(), _DT[x.dtype], tiled.data_ptr(), bits, group, scales.data_ptr(),
+    if _lib is None:
+        load()
+    args = (x.data_ptr(), _DT[x.dtype], tiled.data_ptr(), bits, group, scales.data_ptr(),
             None if zeros is None else zeros.data_ptr(), int(zero_const), out.data_ptr(),
             _DT[out_dtype], M, N, K, _stream(x.get_device()))
+    st = _call14(_ADDR["qmm_gemv_tile16"], *args) if _call14 is not None else _FN["qmm_gemv_tile16"](*args)
     if st:
         raise QmmError(st, "qmm_gemv_tile16")
     return out

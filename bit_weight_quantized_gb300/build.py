@@ -15,6 +15,8 @@ import os
 import shutil
 import subprocess
 import sys
+import sysconfig
+from typing import Optional
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
@@ -90,7 +92,40 @@ def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = Fals
         os.replace(tmp, LIB)
     with open(stamp, "w") as fh:
         fh.write(digest)
+    build_fastcall(verbose)
     return LIB
+
+
+FAST_SRC = os.path.join(CSRC, "pyfast.c")
+
+
+def fastcall_path() -> str:
+    """Where the fast-call extension (csrc/pyfast.c) is built."""
+    return os.path.join(LIBDIR, "_qmmfast" + (sysconfig.get_config_var("EXT_SUFFIX") or ".so"))
+
+
+def build_fastcall(verbose: bool = False) -> Optional[str]:
+    """Compiles the CPython fast-call extension with the host C compiler.  It is
+    optional: without Python's headers (or a compiler) the binding keeps
+    calling through ctypes, so a failure here only warns."""
+    out = fastcall_path()
+    if os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(FAST_SRC):
+        return out
+    inc = sysconfig.get_paths().get("include", "")
+    cc = os.environ.get("CC") or shutil.which("gcc") or shutil.which("cc")
+    if not cc or not os.path.exists(os.path.join(inc, "Python.h")):
+        sys.stderr.write("note: fast-call extension not built (no C compiler or Python.h)\n")
+        return None
+    tmp = out + f".{os.getpid()}.tmp"
+    cmd = [cc, "-O2", "-shared", "-fPIC", "-I", inc, FAST_SRC, "-o", tmp]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        sys.stderr.write(f"note: fast-call extension not built:\n{res.stderr}\n")
+        return None
+    if verbose and res.stderr:
+        sys.stderr.write(res.stderr)
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":
