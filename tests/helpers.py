@@ -34,3 +34,24 @@ def y_to_f64(y: torch.Tensor) -> np.ndarray:
 
 def oracle_y(prob, rows=None, cols=None):
     return oracle.solve_qmm(prob, rows=rows, cols=cols)
+
+
+def weight_rounding_sigma(prob, u, rows=None, cols=None):
+    """Standard deviation of the error that rounding every dequantized weight
+    w = (q - z) * s to the tensor-core operand type adds to y[m][n]: each
+    rounding (RNE) moves w by at most u |w| (u = 2^-8 for bf16), taken as
+    uniform and independent, so the sum's error has standard deviation at
+    most u / sqrt(3) * sqrt(sum_k (x[m][k] w[n][k])^2).  Host-side tolerance
+    arithmetic from the problem's own fields (the expected values come from
+    the oracle)."""
+    x = prob.x_f64()
+    codes = prob.codes.astype(np.float64)
+    s = prob.scales.astype(np.float64)
+    z = (np.full(s.shape, float(prob.zero_const)) if prob.zeros is None
+         else prob.zeros.astype(np.float64))
+    if rows is not None:
+        x = x[rows]
+    if cols is not None:
+        codes, s, z = codes[cols], s[cols], z[cols]
+    w = (codes - np.repeat(z, prob.group, axis=1)) * np.repeat(s, prob.group, axis=1)
+    return u / np.sqrt(3.0) * np.sqrt((x * x) @ (w * w).T)
