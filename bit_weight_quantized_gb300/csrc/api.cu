@@ -143,6 +143,32 @@ bool encode_u16_tmap(CUtensorMap *map, const void *base, long long cols, long lo
     return r == CUDA_SUCCESS;
 }
 
+bool encode_u32_tmap(CUtensorMap *map, const void *base, long long cols, long long rows,
+                     int box_cols, int box_rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 4)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// The canonical decode ring's tensor map, where the plan allows it (else the
+// ring keeps one bulk copy per row).
+static void decode_use_tma(DecodeParams &d)
+{
+    d.tma = 0;
+    if (decode_tma_fits(d.pl, d.row_bytes) &&
+        encode_u32_tmap(&d.tmw, d.packed, d.row_bytes / 4, d.N, d.pl.pitch / 4, kDecodeTmaRows))
+        d.tma = 1;
+}
+
 // Shared checks of qmm_gemv / qmm_gemm (everything that needs no device).
 static qmm_status check_qmm_args(const void *x, const uint8_t *packed, int bits, int group,
                                  const void *scales, int zero_const, const uint8_t *zeros,
@@ -280,6 +306,7 @@ qmm_status qmm_gemv_float(const void *x, const uint8_t *packed, int ebits, int m
         d.mbits = mbits;
         d.fscale = static_cast<float>(1 << (15 - ((1 << (ebits - 1)) - 1)));
         d.pl = plan;
+        decode_use_tma(d);
         return from_cuda(launch_decode_float(d, bits, stream));
     }
     return from_cuda(launch_gemv_fp(static_cast<const uint16_t *>(x), packed, ebits, mbits, group,
@@ -343,6 +370,7 @@ qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int
         d.zero_const = zeros ? 0 : zero_const;
         d.vec_sz = aligned(scales, 16) && (!zeros || aligned(zeros, 8));
         d.pl = plan;
+        decode_use_tma(d);
         return from_cuda(launch_decode(d, bits, false, stream));
     }
 

@@ -52,7 +52,13 @@ bool decode_plan(int M, int N, int K, int group, int bits, bool stored_zeros, bo
             const int bytes = pl.span * pl.seg_bytes;
             // tile16: a slot holds two dense 16-row tiles (fragment reads are contiguous)
             pl.pitch = tile16 ? 0 : bytes + ((pitch_residue(bits) - bytes % 128) + 128) % 128;
-            pl.slot_bytes = tile16 ? 32 * bytes : slot_rows * pl.pitch;
+            // a ring of one-segment slots whose pitch a tensor-map box can span
+            // takes its rows in boxes of 16 (decode_tma_fits): room for whole boxes
+            // (with a single segment the whole-row slot above comes first)
+            const int rows = !tile16 && !whole && pl.pitch <= 1024
+                                 ? min(kRowBlock, align_up(pl.max_rows, kDecodeTmaRows))
+                                 : slot_rows;
+            pl.slot_bytes = tile16 ? 32 * bytes : rows * pl.pitch;
             const int total = nrb * (pl.nseg / pl.span);
             slots = budget > fixed ? (budget - fixed) / pl.slot_bytes : 0;
             slots = slots < total ? slots : total;

@@ -117,9 +117,11 @@ __device__ __forceinline__ void fence_proxy_async_smem()
 // Issues ring chunk i of this CTA (row block i / nchunk, segments
 // [span (i % nchunk), span (i % nchunk + 1))) into its slot, all completing on
 // full[slot].  Canonical layout: one bulk copy of span segments per row, rows
-// at the slot pitch.  Fragment-ordered layout (TILE): one bulk copy per 16-row
-// tile of the row block, the tile's blocks back to back.  Called by all lanes
-// of warp 0.
+// at the slot pitch; or, with the tensor map (p.tma), one box of 16 rows per
+// 16 rows, each row's segment and the pad up to the pitch (the pad holds the
+// next segment's first bytes, or zeros past the row's end, and is never read).
+// Fragment-ordered layout (TILE): one bulk copy per 16-row tile of the row
+// block, the tile's blocks back to back.  Called by all lanes of warp 0.
 template <bool TILE>
 __device__ __forceinline__ void issue_chunk(const DecodeParams &p, uint8_t *slots, uint64_t *full, int i,
                                             int r0, int nrows, uint64_t pol, int lane)
@@ -142,6 +144,14 @@ __device__ __forceinline__ void issue_chunk(const DecodeParams &p, uint8_t *slot
         if (lane < ntiles)
             bulk_load_hint(dst + lane * tbytes, src + lane * 16 * p.row_bytes, static_cast<uint32_t>(tbytes),
                            &full[slot], pol);
+    } else if (p.tma) {
+        const int nbox = (cnt + kDecodeTmaRows - 1) / kDecodeTmaRows;
+        if (lane == 0)
+            mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nbox * kDecodeTmaRows * pl.pitch));
+        __syncwarp();
+        if (lane < nbox)
+            tma_load_2d_hint(dst + lane * kDecodeTmaRows * pl.pitch, &p.tmw, &full[slot], c * (bytes >> 2),
+                             r0 + rr + lane * kDecodeTmaRows, pol);
     } else {
         if (lane == 0)
             mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(cnt * bytes));
@@ -332,7 +342,7 @@ __device__ __noinline__ void stage_rounds(const DecodeParams &p, uint8_t *xw, fl
 // TILE: the weights are in the fragment-ordered (tile16) layout.
 template <int B, int NT, int NB, bool TILE, bool FL>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
-decode_kernel(const DecodeParams p)
+decode_kernel(const __grid_constant__ DecodeParams p)
 {
     const DecodePlan &pl = p.pl;
     extern __shared__ __align__(128) uint8_t smem[];

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace qmm {
@@ -27,6 +28,11 @@ struct DecodePlan {
 };
 
 struct DecodeParams {
+    // canonical layout with one-segment ring slots (tma != 0): a 2-D tensor map
+    // over the packed weights as 32-bit words [N][row_bytes / 4], box pitch / 4
+    // words x 16 rows, so that one copy lands 16 rows at the slot pitch
+    alignas(64) CUtensorMap tmw;
+    int tma;
     const uint16_t *x;        // fp16 or bf16 [M][K], 16-byte aligned
     const uint8_t *packed;    // [N][K*b/8], 16-byte aligned
     const uint16_t *scales;   // fp16 [N][K/G]
@@ -42,6 +48,22 @@ struct DecodeParams {
     float fscale;             // float codes: 2^(15 - bias), folded into the scale
     DecodePlan pl;
 };
+
+// Rows per tensor-map box of the canonical ring (two boxes per 32-row block).
+constexpr int kDecodeTmaRows = 16;
+
+// Whether the canonical ring of `plan` can land its chunks by tensor-map boxes:
+// one-segment slots whose padded pitch is a whole number of 16-byte units of at
+// most 1024 bytes (256 words, the box limit), rows a multiple of 16 bytes, and
+// room in a slot for the 16-row boxes that cover a row block (the planner
+// sizes such slots so).
+inline bool decode_tma_fits(const DecodePlan &plan, long long row_bytes)
+{
+    const int rows = plan.max_rows < 32 ? plan.max_rows : 32;
+    const int boxed = (rows + kDecodeTmaRows - 1) / kDecodeTmaRows * kDecodeTmaRows;
+    return plan.span == 1 && plan.pitch % 16 == 0 && plan.pitch <= 1024 && row_bytes % 16 == 0 &&
+           plan.seg_bytes % 16 == 0 && plan.slot_bytes >= boxed * plan.pitch;
+}
 
 // Plans a call; false if the kernel does not take the shape (the skinny kernel
 // does).  smem_pair is the per-CTA shared memory with which two CTAs share an
