@@ -143,17 +143,17 @@ bool encode_u16_tmap(CUtensorMap *map, const void *base, long long cols, long lo
     return r == CUDA_SUCCESS;
 }
 
-bool encode_u32_tmap(CUtensorMap *map, const void *base, long long cols, long long rows,
+bool encode_u64_tmap(CUtensorMap *map, const void *base, long long cols, long long rows,
                      int box_cols, int box_rows)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc)
         return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 4)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 8)};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base), dims,
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(base), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -165,7 +165,7 @@ static void decode_use_tma(DecodeParams &d)
 {
     d.tma = 0;
     if (decode_tma_fits(d.pl, d.row_bytes) &&
-        encode_u32_tmap(&d.tmw, d.packed, d.row_bytes / 4, d.N, d.pl.pitch / 4, kDecodeTmaRows))
+        encode_u64_tmap(&d.tmw, d.packed, d.row_bytes / 8, d.N, d.pl.pitch / 8, decode_tma_rows(d.pl)))
         d.tma = 1;
 }
 

@@ -52,13 +52,10 @@ bool decode_plan(int M, int N, int K, int group, int bits, bool stored_zeros, bo
             const int bytes = pl.span * pl.seg_bytes;
             // tile16: a slot holds two dense 16-row tiles (fragment reads are contiguous)
             pl.pitch = tile16 ? 0 : bytes + ((pitch_residue(bits) - bytes % 128) + 128) % 128;
-            // a ring of one-segment slots whose pitch a tensor-map box can span
-            // takes its rows in boxes of 16 (decode_tma_fits): room for whole boxes
-            // (with a single segment the whole-row slot above comes first)
-            const int rows = !tile16 && !whole && pl.pitch <= 1024
-                                 ? min(kRowBlock, align_up(pl.max_rows, kDecodeTmaRows))
-                                 : slot_rows;
-            pl.slot_bytes = tile16 ? 32 * bytes : rows * pl.pitch;
+            pl.slot_bytes = tile16 ? 32 * bytes : slot_rows * pl.pitch;
+            // slots a tensor-map box fills (decode_tma_fits) start on 128 bytes
+            if (!tile16 && pl.pitch <= 2048)
+                pl.slot_bytes = align_up(pl.slot_bytes, 128);
             const int total = nrb * (pl.nseg / pl.span);
             slots = budget > fixed ? (budget - fixed) / pl.slot_bytes : 0;
             slots = slots < total ? slots : total;

@@ -117,9 +117,10 @@ __device__ __forceinline__ void fence_proxy_async_smem()
 // Issues ring chunk i of this CTA (row block i / nchunk, segments
 // [span (i % nchunk), span (i % nchunk + 1))) into its slot, all completing on
 // full[slot].  Canonical layout: one bulk copy of span segments per row, rows
-// at the slot pitch; or, with the tensor map (p.tma), one box of 16 rows per
-// 16 rows, each row's segment and the pad up to the pitch (the pad holds the
-// next segment's first bytes, or zeros past the row's end, and is never read).
+// at the slot pitch; or, with the tensor map (p.tma), one box of a slot's rows,
+// each row's chunk and the pad up to the pitch (the pad holds the next
+// segment's first bytes, or zeros past the row's end, and is never read; rows
+// past the CTA's last belong to the next CTA or are zeros, and are not used).
 // Fragment-ordered layout (TILE): one bulk copy per 16-row tile of the row
 // block, the tile's blocks back to back.  Called by all lanes of warp 0.
 template <bool TILE>
@@ -144,14 +145,12 @@ __device__ __forceinline__ void issue_chunk(const DecodeParams &p, uint8_t *slot
         if (lane < ntiles)
             bulk_load_hint(dst + lane * tbytes, src + lane * 16 * p.row_bytes, static_cast<uint32_t>(tbytes),
                            &full[slot], pol);
-    } else if (p.tma) {
-        const int nbox = (cnt + kDecodeTmaRows - 1) / kDecodeTmaRows;
-        if (lane == 0)
-            mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nbox * kDecodeTmaRows * pl.pitch));
+    } else if (p.tma && (smem_u32(dst) & 127u) == 0) {   // a tensor copy lands on 128 bytes
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(decode_tma_rows(pl) * pl.pitch));
+            tma_load_2d_hint(dst, &p.tmw, &full[slot], c * (bytes >> 3), r0 + rr, pol);
+        }
         __syncwarp();
-        if (lane < nbox)
-            tma_load_2d_hint(dst + lane * kDecodeTmaRows * pl.pitch, &p.tmw, &full[slot], c * (bytes >> 2),
-                             r0 + rr + lane * kDecodeTmaRows, pol);
     } else {
         if (lane == 0)
             mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(cnt * bytes));

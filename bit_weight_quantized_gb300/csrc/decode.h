@@ -28,9 +28,9 @@ struct DecodePlan {
 };
 
 struct DecodeParams {
-    // canonical layout with one-segment ring slots (tma != 0): a 2-D tensor map
-    // over the packed weights as 32-bit words [N][row_bytes / 4], box pitch / 4
-    // words x 16 rows, so that one copy lands 16 rows at the slot pitch
+    // canonical layout (tma != 0): a 2-D tensor map over the packed weights as
+    // 64-bit words [N][row_bytes / 8], box pitch / 8 words x min(32, max_rows)
+    // rows, so that one copy lands a ring chunk's rows at the slot pitch
     alignas(64) CUtensorMap tmw;
     int tma;
     const uint16_t *x;        // fp16 or bf16 [M][K], 16-byte aligned
@@ -49,21 +49,18 @@ struct DecodeParams {
     DecodePlan pl;
 };
 
-// Rows per tensor-map box of the canonical ring (two boxes per 32-row block).
-constexpr int kDecodeTmaRows = 16;
-
-// Whether the canonical ring of `plan` can land its chunks by tensor-map boxes:
-// one-segment slots whose padded pitch is a whole number of 16-byte units of at
-// most 1024 bytes (256 words, the box limit), rows a multiple of 16 bytes, and
-// room in a slot for the 16-row boxes that cover a row block (the planner
-// sizes such slots so).
+// Whether the canonical ring of `plan` can land each chunk with one tensor-map
+// box: a padded pitch that is a whole number of 16-byte units of at most 2048
+// bytes (256 64-bit words, the box limit) and chunks that start on 16 bytes.
+// The box covers min(32, max_rows) rows, exactly a slot.
 inline bool decode_tma_fits(const DecodePlan &plan, long long row_bytes)
 {
-    const int rows = plan.max_rows < 32 ? plan.max_rows : 32;
-    const int boxed = (rows + kDecodeTmaRows - 1) / kDecodeTmaRows * kDecodeTmaRows;
-    return plan.span == 1 && plan.pitch % 16 == 0 && plan.pitch <= 1024 && row_bytes % 16 == 0 &&
-           plan.seg_bytes % 16 == 0 && plan.slot_bytes >= boxed * plan.pitch;
+    return plan.pitch > 0 && plan.pitch % 16 == 0 && plan.pitch <= 2048 && row_bytes % 16 == 0 &&
+           (static_cast<long long>(plan.span) * plan.seg_bytes) % 16 == 0;
 }
+
+// Rows of the canonical ring's tensor-map box (a slot's rows).
+__host__ __device__ inline int decode_tma_rows(const DecodePlan &plan) { return plan.max_rows < 32 ? plan.max_rows : 32; }
 
 // Plans a call; false if the kernel does not take the shape (the skinny kernel
 // does).  smem_pair is the per-CTA shared memory with which two CTAs share an

@@ -80,9 +80,9 @@ bool encode_byte_tmap(CUtensorMap *map, const void *base, long long row_bytes, l
                       int box_cols, int box_rows, bool swizzle128);
 bool encode_u16_tmap(CUtensorMap *map, const void *base, long long cols, long long rows,
                      int box_cols, int box_rows);
-// And over a matrix of 32-bit words [rows][cols], unswizzled, zero-filled
-// outside (row pitch cols * 4 bytes).
-bool encode_u32_tmap(CUtensorMap *map, const void *base, long long cols, long long rows,
+// And over a matrix of 64-bit words [rows][cols], unswizzled, zero-filled
+// outside (row pitch cols * 8 bytes).
+bool encode_u64_tmap(CUtensorMap *map, const void *base, long long cols, long long rows,
                      int box_cols, int box_rows);
 
 }  // namespace qmm

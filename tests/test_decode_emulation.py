@@ -265,11 +265,11 @@ def _emulate_staged(prob, packed, plan, tile16=False):
         nrb = -(-nrows // 32)
         span = plan["span"]
         chunk = span * plan["seg_bytes"]
-        # the rule of decode_tma_fits (decode.h): one-segment slots with room for
-        # whole 16-row boxes take their chunks by tensor-map boxes
-        boxed = -(-min(32, plan["max_rows"]) // 16) * 16
-        tma = (not tile16 and span == 1 and pitch % 16 == 0 and pitch <= 1024 and row_bytes % 16 == 0
-               and plan["seg_bytes"] % 16 == 0 and slot_bytes >= boxed * pitch)
+        # the rule of decode_tma_fits (decode.h): one tensor-map box of a slot's
+        # rows per chunk where the pitch is at most 2048 bytes
+        box_rows = min(32, plan["max_rows"])
+        tma = (not tile16 and pitch % 16 == 0 and 0 < pitch <= 2048 and row_bytes % 16 == 0
+               and chunk % 16 == 0)
         for rb in range(nrb):
             rr = 32 * rb
             cnt = min(32, nrows - rr)
@@ -286,18 +286,16 @@ def _emulate_staged(prob, packed, plan, tile16=False):
                         src = (r0 + rr) * row_bytes + c * 16 * chunk + ti * 16 * row_bytes
                         assert src + 16 * chunk <= packed.size
                         sm[dst:dst + 16 * chunk] = packed.reshape(-1)[src:src + 16 * chunk]
-                elif jj == 0 and tma:   # tensor-map boxes of 16 rows x pitch bytes (zeros outside)
+                elif jj == 0 and tma:   # one tensor-map box: a slot's rows x pitch bytes (zeros outside)
                     flat = packed.reshape(-1)
-                    for ti in range(-(-cnt // 16)):
-                        dst = base + ti * 16 * pitch
-                        assert dst % 128 == 0 and (c * chunk) % 16 == 0
-                        assert dst + 16 * pitch <= base + slot_bytes <= plan["off_x"]
-                        for r in range(16):
-                            row = r0 + rr + 16 * ti + r
-                            n = max(0, min(pitch, row_bytes - c * chunk)) if row < N else 0
-                            src = row * row_bytes + c * chunk
-                            sm[dst + r * pitch:dst + r * pitch + pitch] = 0
-                            sm[dst + r * pitch:dst + r * pitch + n] = flat[src:src + n]
+                    assert base % 128 == 0 and (c * chunk) % 16 == 0 and box_rows >= cnt
+                    assert base + box_rows * pitch <= base + slot_bytes <= plan["off_x"]
+                    for r in range(box_rows):
+                        row = r0 + rr + r
+                        n = max(0, min(pitch, row_bytes - c * chunk)) if row < N else 0
+                        src = row * row_bytes + c * chunk
+                        sm[base + r * pitch:base + (r + 1) * pitch] = 0
+                        sm[base + r * pitch:base + r * pitch + n] = flat[src:src + n]
                 elif jj == 0:   # the chunk's bulk copies: one per row
                     for r in range(cnt):
                         dst = base + r * pitch
@@ -410,17 +408,17 @@ def test_staged_kernel_emulation_small_ring(tmp_path):
     (6, 4, 40, 4096, 64, "group", 95000), (4, 2, 25, 8192, 128, "half", 75000),
     (8, 1, 37, 2048, 64, "group", 60000), (3, 16, 70, 4096, 64, "const8", 196000)])
 def test_staged_kernel_emulation_tma_boxes(b, M, N, K, G, zm, budget, tmp_path):
-    # one-segment ring slots landed by 16-row tensor-map boxes (the canonical
-    # layout's rule in decode.h): each box stays inside its slot, rows past N and
-    # bytes past a row's end arrive as zeros, and the result is the oracle's
+    # one-segment ring slots landed by one tensor-map box each (the canonical
+    # layout's rule in decode.h; the other emulation cases take it too where the
+    # pitch allows): each box stays inside its slot, rows past N and bytes past a
+    # row's end arrive as zeros, and the result is the oracle's
     import oracle
     import synthetic
     from tests.test_planner import decode_plans
     prob = synthetic.make_qmm(M, N, K, b, G, zero_mode=zm, seed=b + 5 * M)
     plan = decode_plans([(M, N, K, G, b, 1 if prob.zeros is not None else 0, 1, budget, budget)],
                         tmp_path)[0]
-    assert plan is not None and plan["span"] == 1 and plan["pitch"] <= 1024
-    assert plan["slot_bytes"] >= -(-min(32, plan["max_rows"]) // 16) * 16 * plan["pitch"]
+    assert plan is not None and plan["span"] == 1 and plan["pitch"] <= 2048
     y = _emulate_staged(prob, oracle.pack(prob.codes, b)[0], plan)
     ref = oracle.solve_qmm(prob)
     np.testing.assert_allclose(y, ref, rtol=0, atol=1e-9 * max(1.0, np.abs(ref).max()))

@@ -210,10 +210,11 @@ def test_decode_plan_layout(dplans):
         assert pl["pitch"] >= chunk and pl["pitch"] % 16 == 0, key
         assert pl["pitch"] % 128 == resid[b], key
         slot_rows = min(32, pl["max_rows"])
-        if pl["span"] == 1 and pl["nseg"] > 1 and pl["pitch"] <= 1024:
-            # a ring of one-segment slots a tensor-map box can span: room for whole 16-row boxes
-            slot_rows = min(32, _ceil(pl["max_rows"], 16) * 16)
-        assert pl["slot_bytes"] == slot_rows * pl["pitch"], key
+        if pl["pitch"] <= 2048:
+            # slots that one tensor-map box fills start on 128 bytes
+            assert pl["slot_bytes"] == _ceil(slot_rows * pl["pitch"], 128) * 128, key
+        else:
+            assert pl["slot_bytes"] == slot_rows * pl["pitch"], key
         total = _ceil(pl["max_rows"], 32) * (pl["nseg"] // pl["span"])
         assert 1 <= pl["slots"] <= min(total, 16), key
         assert pl["slots"] == total or pl["slots"] >= 2, key
