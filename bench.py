@@ -694,14 +694,14 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-PROFILE_FAMILIES = ("skinny_tile16_m16", "w4a8_m64", "tiled_m128")
+PROFILE_FAMILIES = ("skinny_m16", "skinny_tile16_m16", "w4a8_m64", "tiled_m128")
 
 
 def run_profile_family(name: str, launches: int = 4):
     """A few eager calls of one workload family on device-generated inputs, for
-    a profiler to capture one of them: the skinny batched decode on the
-    fragment-ordered layout (M = 16, N = 14336, K = 4096, b = 6, group 64,
-    stored zeros), W4A8 at M = 64 (K = N = 4096, group 128) or the tiled path at
+    a profiler to capture one of them: the skinny batched decode (M = 16,
+    N = 14336, K = 4096, b = 6, group 64, stored zeros) on the canonical or the
+    fragment-ordered layout, W4A8 at M = 64 (K = N = 4096, group 128) or the tiled path at
     M = 128 (K = 8192, N = 28672, int4, bf16)."""
     import torch
     import bit_weight_quantized_gb300 as q
@@ -709,7 +709,14 @@ def run_profile_family(name: str, launches: int = 4):
     dev = torch.device("cuda:0")
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
-    if name == "skinny_tile16_m16":
+    if name == "skinny_m16":
+        M, N, K, b, G = 16, 14336, 4096, 6, 64
+        pk = q.qmm_pack(torch.randint(0, 1 << b, (N, K), dtype=torch.uint8, device=dev, generator=gen), b)
+        sc = (0.02 * torch.randn(N, K // G, device=dev, generator=gen).abs() + 1e-3).half()
+        zz = torch.randint(0, 1 << b, (N, K // G), dtype=torch.uint8, device=dev, generator=gen)
+        x = torch.randn(M, K, device=dev, generator=gen).half()
+        call = lambda: q.qmm_gemv(x, pk, b, G, sc, zz)
+    elif name == "skinny_tile16_m16":
         M, N, K, b, G = 16, 14336, 4096, 6, 64
         tiled = q.qmm_repack(q.qmm_pack(torch.randint(0, 1 << b, (N, K), dtype=torch.uint8, device=dev,
                                                       generator=gen), b), K, b, "tile16")
