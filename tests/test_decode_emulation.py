@@ -261,7 +261,7 @@ def _emulate_staged(prob, packed, plan, tile16=False):
                             sm[dst:dst + 32] = run[slot_code].view(np.uint8)
                             X[w, m, j] += xf[m, src:src + 16].sum()
                             C[w, m, j] += (pw * xf[m, src:src + 16]).sum()
-        assert plan["off_xsum"] + W * M * nseg * 4 <= plan["off_sc"]
+        assert plan["off_xsum"] + W * M * nseg * 8 <= plan["off_sc"]   # (X, C) fp32 pairs
         nrb = -(-nrows // 32)
         span = plan["span"]
         chunk = span * plan["seg_bytes"]

@@ -224,7 +224,7 @@ def test_decode_plan_layout(dplans):
         assert pl["slots"] * pl["slot_bytes"] <= pl["off_x"] and pl["off_x"] % 16 == 0, key
         assert pl["x_pitch"] == K // pl["warps"] * 2 + 16, key
         assert pl["off_x"] + pl["warps"] * M * pl["x_pitch"] <= pl["off_xsum"], key
-        assert pl["off_xsum"] + pl["warps"] * M * pl["nseg"] * 4 <= pl["off_sc"], key
+        assert pl["off_xsum"] + pl["warps"] * M * pl["nseg"] * 8 <= pl["off_sc"], key   # (X, C) pairs
         ng = K // G
         assert pl["off_sc"] + pl["max_rows"] * ng * 2 <= pl["off_zo"], key
         assert pl["off_zo"] + (pl["max_rows"] * ng * 2 if z else 0) <= pl["off_red"], key
