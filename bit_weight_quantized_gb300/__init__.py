@@ -285,7 +285,8 @@ GEMV_KERNELS = {"auto": 0, "skinny": 1}
 def qmm_set_gemv_kernel(kernel: str):
     """Kernel choice of qmm_gemv for the calls that follow, process-wide:
     "auto" (the decode kernel where it applies, else the skinny kernel) or
-    "skinny" (the skinny kernel for every shape)."""
+    "skinny" (the skinny kernel for every shape; qmm_w4a8 / qmm_w8a8 then stay
+    off the decode kernel too)."""
     if kernel not in GEMV_KERNELS:
         raise ValueError(f"kernel must be one of {sorted(GEMV_KERNELS)}")
     _check(load().qmm_set_gemv_kernel(GEMV_KERNELS[kernel]), "qmm_set_gemv_kernel")

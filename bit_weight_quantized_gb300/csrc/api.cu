@@ -159,16 +159,6 @@ bool encode_u64_tmap(CUtensorMap *map, const void *base, long long cols, long lo
     return r == CUDA_SUCCESS;
 }
 
-// The canonical decode ring's tensor map, where the plan allows it (else the
-// ring keeps one bulk copy per row).
-static void decode_use_tma(DecodeParams &d)
-{
-    d.tma = 0;
-    if (decode_tma_fits(d.pl, d.row_bytes) &&
-        encode_u64_tmap(&d.tmw, d.packed, d.row_bytes / 8, d.N, d.pl.pitch / 8, decode_tma_rows(d.pl)))
-        d.tma = 1;
-}
-
 // Shared checks of qmm_gemv / qmm_gemm (everything that needs no device).
 static qmm_status check_qmm_args(const void *x, const uint8_t *packed, int bits, int group,
                                  const void *scales, int zero_const, const uint8_t *zeros,
@@ -306,7 +296,7 @@ qmm_status qmm_gemv_float(const void *x, const uint8_t *packed, int ebits, int m
         d.mbits = mbits;
         d.fscale = static_cast<float>(1 << (15 - ((1 << (ebits - 1)) - 1)));
         d.pl = plan;
-        decode_use_tma(d);
+        decode_set_tma(d);
         return from_cuda(launch_decode_float(d, bits, stream));
     }
     return from_cuda(launch_gemv_fp(static_cast<const uint16_t *>(x), packed, ebits, mbits, group,
@@ -370,7 +360,7 @@ qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int
         d.zero_const = zeros ? 0 : zero_const;
         d.vec_sz = aligned(scales, 16) && (!zeros || aligned(zeros, 8));
         d.pl = plan;
-        decode_use_tma(d);
+        decode_set_tma(d);
         return from_cuda(launch_decode(d, bits, false, stream));
     }
 
@@ -563,7 +553,8 @@ qmm_status qmm_w4a8(const int8_t *xq, const void *sa, const uint8_t *w4, const v
         return from_cuda(e);
     }
     return wxa8_dispatch(4, xq, sa, w4, ws, group, y, acc_out, M, N, K, f->status, f->num_sms,
-                         f->smem_optin, f->smem_pair, stream);
+                         f->smem_optin, f->smem_pair,
+                         g_gemv_kernel.load(std::memory_order_relaxed) == QMM_GEMV_AUTO, stream);
 }
 
 qmm_status qmm_w8a8(const int8_t *xq, const void *sa, const int8_t *w8, const void *ws,
@@ -591,7 +582,8 @@ qmm_status qmm_w8a8(const int8_t *xq, const void *sa, const int8_t *w8, const vo
     if (K == 0)
         return from_cuda(cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * 2, stream));
     return wxa8_dispatch(8, xq, sa, reinterpret_cast<const uint8_t *>(w8), ws, group, y, acc_out, M, N,
-                         K, f->status, f->num_sms, f->smem_optin, f->smem_pair, stream);
+                         K, f->status, f->num_sms, f->smem_optin, f->smem_pair,
+                         g_gemv_kernel.load(std::memory_order_relaxed) == QMM_GEMV_AUTO, stream);
 }
 
 qmm_status qmm_quantize_act(const void *x, int8_t *xq, void *sa, int M, int K, cudaStream_t stream)

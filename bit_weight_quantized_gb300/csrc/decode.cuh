@@ -209,7 +209,16 @@ __device__ __forceinline__ void extract_float_run(const uint32_t (&w)[run_words<
     }
 }
 
-template <int B, int NT, bool FL>
+// The fp16 bits of the pair (2^E_lo, 2^E_hi) that the integer plans add to the
+// codes of pair q of a run (slot order), for the exact-integer mode.
+template <int B>
+__host__ __device__ constexpr uint32_t offset_pair(int q)
+{
+    return static_cast<uint32_t>(exp_of_code<B, 16>(code_of_slot<B, 16>(2 * q)) + 15) << 10 |
+           static_cast<uint32_t>(exp_of_code<B, 16>(code_of_slot<B, 16>(2 * q + 1)) + 15) << 26;
+}
+
+template <int B, int NT, bool FL, bool IX = false>
 __device__ __forceinline__ void block_mma(const uint8_t *const (&run0)[2][2], int boff, const uint8_t *xb,
                                           int x_pitch, int m0, int m1, int o, uint3 fl, float (&acc)[2][2][NT][4])
 {
@@ -221,10 +230,20 @@ __device__ __forceinline__ void block_mma(const uint8_t *const (&run0)[2][2], in
         for (int h = 0; h < 2; ++h) {
             uint32_t w[NW];
             load_run<B>(w, run0[i][h] + boff, o);
+            if constexpr (IX) {   // signed codes: two's complement -> offset binary (c xor 2^(b-1))
+#pragma unroll
+                for (int k = 0; k < NW; ++k)
+                    w[k] ^= B == 4 ? 0x88888888u : 0x80808080u;
+            }
             if constexpr (FL)
                 extract_float_run<B>(w, fl, a[i][h]);
             else
                 extract_run<B, 16, false, false>(w, a[i][h]);
+            if constexpr (IX) {   // 2^E + u - 2^E: the code u itself, so that every sum stays exact
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    a[i][h][q] = hsub2(a[i][h][q], offset_pair<B>(q));
+            }
         }
     uint32_t xw[NT][8];
 #pragma unroll
@@ -250,11 +269,22 @@ __device__ __forceinline__ void block_mma(const uint8_t *const (&run0)[2][2], in
 // order) in fragment (slot) order: slot s of the run holds x of the run's code
 // code_of_slot(s).  Returns the run's sums X = sum x and C = sum 2^E x (E of
 // each code's position in the plan), in fp32.
-template <int B, bool FL>
+template <int B, bool FL, bool IX = false>
 __device__ __forceinline__ float2 stage_run(uint8_t *dst, const uint4 (&raw)[2], bool x_bf16)
 {
     uint32_t in[8] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w};
-    if (x_bf16) {
+    if constexpr (IX) {
+        // 16 int8 activations (raw[0]) as exact fp16 pairs: byte v + 128 under
+        // the fp16 exponent byte 0x64 reads 1152 + v; minus 1152 leaves v
+        const uint32_t wv[4] = {raw[0].x ^ 0x80808080u, raw[0].y ^ 0x80808080u, raw[0].z ^ 0x80808080u,
+                                raw[0].w ^ 0x80808080u};
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const uint32_t b0 = static_cast<uint32_t>(2 * (q & 1));
+            in[q] = hsub2(prmt(wv[q >> 1], 0x64646464u, b0 | (4u << 4) | ((b0 + 1u) << 8) | (4u << 12)),
+                          0x64806480u);
+        }
+    } else if (x_bf16) {
         // bf16 activations become fp16: exact for magnitudes in [2^-14, 65504]
         // (8 significant bits fit in 11), rounded to the fp16 subnormal grid below
 #pragma unroll
@@ -280,7 +310,7 @@ __device__ __forceinline__ float2 stage_run(uint8_t *dst, const uint4 (&raw)[2],
     for (int c = 0; c < 16; ++c) {
         const float v = f16_bits_to_f32(static_cast<uint16_t>(in[c >> 1] >> (16 * (c & 1))));
         X += v;
-        if constexpr (!FL)   // float codes carry no offset
+        if constexpr (!FL && !IX)   // float codes carry no offset, exact-integer operands neither
             C = fmaf(static_cast<float>(1 << exp_of_code<B, 16>(c)), v, C);
     }
     return make_float2(X, C);
@@ -288,7 +318,7 @@ __device__ __forceinline__ float2 stage_run(uint8_t *dst, const uint4 (&raw)[2],
 
 // The activation staging of more than one round (several tokens or long K),
 // kept out of line so that the one-round path of the decode shapes stays compact.
-template <int B, int NB, bool FL>
+template <int B, int NB, bool FL, bool IX = false>
 __device__ __noinline__ void stage_rounds(const DecodeParams &p, uint8_t *xw, float2 *xs, int warp, int lane,
                                           int rounds)
 {
@@ -304,7 +334,12 @@ __device__ __noinline__ void stage_rounds(const DecodeParams &p, uint8_t *xw, fl
             for (int q = 0; q < kBatch; ++q) {
                 mq[q] = mr;
                 jq[q] = r0 + q < rounds ? jr + jl : pl.nseg;   // nseg marks an idle lane
-                if (jq[q] < pl.nseg) {
+                if (jq[q] < pl.nseg && IX) {   // 16 int8 activations
+                    const int8_t *src = reinterpret_cast<const int8_t *>(p.x) + static_cast<long long>(mq[q]) * p.K +
+                                        jq[q] * pl.kseg + 64 * (warp * NB + bb) + 16 * tq;
+                    raw[q][0] = *reinterpret_cast<const uint4 *>(src);
+                    raw[q][1] = make_uint4(0u, 0u, 0u, 0u);
+                } else if (jq[q] < pl.nseg) {
                     const uint16_t *src = p.x + static_cast<long long>(mq[q]) * p.K + jq[q] * pl.kseg +
                                           64 * (warp * NB + bb) + 16 * tq;
                     raw[q][0] = *reinterpret_cast<const uint4 *>(src);
@@ -324,7 +359,7 @@ __device__ __noinline__ void stage_rounds(const DecodeParams &p, uint8_t *xw, fl
                     break;
                 float2 v = make_float2(0.f, 0.f);
                 if (jq[q] < pl.nseg)
-                    v = stage_run<B, FL>(xw + mq[q] * pl.x_pitch + ((jq[q] * NB + bb) * 64 + 16 * tq) * 2, raw[q],
+                    v = stage_run<B, FL, IX>(xw + mq[q] * pl.x_pitch + ((jq[q] * NB + bb) * 64 + 16 * tq) * 2, raw[q],
                                      p.x_bf16 != 0);
 #pragma unroll
                 for (int off = 1; off < 4 * NB; off <<= 1) {
@@ -339,7 +374,7 @@ __device__ __noinline__ void stage_rounds(const DecodeParams &p, uint8_t *xw, fl
 
 // NB = G / 64 blocks per group; warp w owns group w of every 8-group segment.
 // TILE: the weights are in the fragment-ordered (tile16) layout.
-template <int B, int NT, int NB, bool TILE, bool FL>
+template <int B, int NT, int NB, bool TILE, bool FL, bool IX = false>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
 decode_kernel(const __grid_constant__ DecodeParams p)
 {
@@ -455,10 +490,17 @@ decode_kernel(const __grid_constant__ DecodeParams p)
         if (rounds == 1) {   // one round (a single token and at most jstep segments)
             float2 v = make_float2(0.f, 0.f);
             if (jl < pl.nseg) {
-                const uint16_t *src = p.x + jl * pl.kseg + 64 * (warp * NB + bb) + 16 * tq;
-                const uint4 raw[2] = {*reinterpret_cast<const uint4 *>(src),
-                                      *reinterpret_cast<const uint4 *>(src + 8)};
-                v = stage_run<B, FL>(xw + ((jl * NB + bb) * 64 + 16 * tq) * 2, raw, p.x_bf16 != 0);
+                uint4 raw[2];
+                if constexpr (IX) {   // 16 int8 activations
+                    raw[0] = *reinterpret_cast<const uint4 *>(reinterpret_cast<const int8_t *>(p.x) + jl * pl.kseg +
+                                                              64 * (warp * NB + bb) + 16 * tq);
+                    raw[1] = make_uint4(0u, 0u, 0u, 0u);
+                } else {
+                    const uint16_t *src = p.x + jl * pl.kseg + 64 * (warp * NB + bb) + 16 * tq;
+                    raw[0] = *reinterpret_cast<const uint4 *>(src);
+                    raw[1] = *reinterpret_cast<const uint4 *>(src + 8);
+                }
+                v = stage_run<B, FL, IX>(xw + ((jl * NB + bb) * 64 + 16 * tq) * 2, raw, p.x_bf16 != 0);
             }
 #pragma unroll
             for (int off = 1; off < 4 * NB; off <<= 1) {
@@ -469,7 +511,7 @@ decode_kernel(const __grid_constant__ DecodeParams p)
                 xs[jl] = v;
         }
         if (rounds > 1)
-            stage_rounds<B, NB, FL>(p, xw, xs, warp, lane, rounds);
+            stage_rounds<B, NB, FL, IX>(p, xw, xs, warp, lane, rounds);
         __syncwarp();
     }
 
@@ -540,7 +582,7 @@ decode_kernel(const __grid_constant__ DecodeParams p)
                         // block kblock of the chunk: 8 b bytes apart per row (canonical), or one
                         // 16-row unit of 128 b bytes apart (tile16)
                         const int kblock = jj * (pl.kseg / 64) + warp * NB + bb;
-                        block_mma<B, NT, FL>(run0, kblock * (TILE ? 128 * B : 8 * B),
+                        block_mma<B, NT, FL, IX>(run0, kblock * (TILE ? 128 * B : 8 * B),
                                              xw + ((j * NB + bb) * 64 + 16 * t) * 2, pl.x_pitch, m0, m1, o, fl,
                                              acc);
                     }
@@ -571,6 +613,23 @@ decode_kernel(const __grid_constant__ DecodeParams p)
                                         s, fmaf(-z, X[tt][cc], (NT == 2 ? acc[0][i][tt][2 * h + cc] + acc[1][i][tt][2 * h + cc]
                                                                         : acc[0][i][tt][2 * h + cc]) - D[tt][cc]),
                                     tot[i][tt][2 * h + cc]);
+                            if constexpr (IX) {
+                                // the exact integer accumulator sum (u - z) x of the group, when asked
+                                const int row = 16 * i + 8 * h + g;
+                                if (p.acc_out && row < cnt) {
+#pragma unroll
+                                    for (int tt = 0; tt < NT; ++tt)
+#pragma unroll
+                                        for (int cc = 0; cc < 2; ++cc) {
+                                            const int tok = 8 * tt + 2 * t + cc;
+                                            const float a = (NT == 2 ? acc[0][i][tt][2 * h + cc] + acc[1][i][tt][2 * h + cc]
+                                                                     : acc[0][i][tt][2 * h + cc]) - D[tt][cc];
+                                            if (tok < p.M)
+                                                p.acc_out[(static_cast<long long>(tok) * p.N + r0 + rr + row) * ng + gidx] =
+                                                    static_cast<int32_t>(a);
+                                        }
+                                }
+                            }
                         }
                 }
             }
@@ -617,6 +676,8 @@ decode_kernel(const __grid_constant__ DecodeParams p)
             for (int w = 0; w < kWarps; ++w)
                 v += red[(w * kRowBlock + row) * p.M + tok];
             const long long out = static_cast<long long>(tok) * p.N + r0 + rr + row;
+            if constexpr (IX)   // the per-token activation scale
+                v *= f16_bits_to_f32(p.sa[tok]);
             reinterpret_cast<uint16_t *>(p.y)[out] = p.y_bf16 ? f32_to_bf16_bits(v) : f32_to_f16_bits(v);
         }
         if (rb + 1 < nrb)
@@ -632,10 +693,10 @@ decode_kernel(const __grid_constant__ DecodeParams p)
     }
 }
 
-template <int B, int NT, int NB, bool TILE, bool FL>
+template <int B, int NT, int NB, bool TILE, bool FL, bool IX = false>
 cudaError_t launch_decode_b(const DecodeParams &p, cudaStream_t stream)
 {
-    auto kern = decode_kernel<B, NT, NB, TILE, FL>;
+    auto kern = decode_kernel<B, NT, NB, TILE, FL, IX>;
     static SmemLimit limit;
     if (const cudaError_t e = ensure_smem_limit(limit, kern, p.pl.smem, true); e != cudaSuccess)
         return e;
@@ -676,6 +737,18 @@ cudaError_t launch_decode_layout(const DecodeParams &p, int bits, cudaStream_t s
     if (p.M > 8)
         return g128 ? launch_decode_cfg<2, 2, TILE>(p, bits, stream) : launch_decode_cfg<2, 1, TILE>(p, bits, stream);
     return g128 ? launch_decode_cfg<1, 2, TILE>(p, bits, stream) : launch_decode_cfg<1, 1, TILE>(p, bits, stream);
+}
+
+// Exact-integer mode (int8 activations, signed b-bit weights), every configuration.
+template <int B>
+cudaError_t launch_decode_int_width(const DecodeParams &p, cudaStream_t stream)
+{
+    const bool g128 = p.group_log2 == 7;
+    if (p.M > 8)
+        return g128 ? launch_decode_b<B, 2, 2, false, false, true>(p, stream)
+                    : launch_decode_b<B, 2, 1, false, false, true>(p, stream);
+    return g128 ? launch_decode_b<B, 1, 2, false, false, true>(p, stream)
+                : launch_decode_b<B, 1, 1, false, false, true>(p, stream);
 }
 
 // Float codes of width B (canonical layout), every configuration.

@@ -46,6 +46,11 @@ struct DecodeParams {
     int vec_sz;               // scales 16-byte and zeros 8-byte aligned: vector staging
     int ebits, mbits;         // float codes: exponent and mantissa bits (0 for integer codes)
     float fscale;             // float codes: 2^(15 - bias), folded into the scale
+    // exact-integer mode (qmm_w4a8 / qmm_w8a8): x holds int8 [M][K], zero_const
+    // is 2^(b-1), y = sa[m] * sum_g s * acc, and the int32 accumulators go to
+    // acc_out [M][N][K/G] when it is not null
+    const uint16_t *sa;       // fp16 [M] per-token activation scales
+    int32_t *acc_out;
     DecodePlan pl;
 };
 
@@ -72,7 +77,12 @@ bool decode_plan(int M, int N, int K, int group, int bits, bool stored_zeros, bo
 // tile16: the weights are in the fragment-ordered layout (qmm_repack).
 cudaError_t launch_decode(const DecodeParams &p, int bits, bool tile16, cudaStream_t stream);
 cudaError_t launch_decode_tile16(const DecodeParams &p, int bits, cudaStream_t stream);
-// Float codes (qmm_gemv_float): bits 4 or 8, at most 4 exponent bits.
+// Float codes (qmm_gemv_float): bits 2..8, at most 4 exponent bits.
 cudaError_t launch_decode_float(const DecodeParams &p, int bits, cudaStream_t stream);
+// Exact-integer mode (decode_int.cu): int8 activations, signed 4- or 8-bit weights.
+cudaError_t launch_decode_int(const DecodeParams &p, int bits, cudaStream_t stream);
+// Sets p.tma and p.tmw when the canonical ring can land its chunks by
+// tensor-map boxes (decode_tma_fits); host code, in decode_int.cu.
+void decode_set_tma(DecodeParams &p);
 
 }  // namespace qmm

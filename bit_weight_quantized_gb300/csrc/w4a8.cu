@@ -10,6 +10,7 @@
 // (signed int8 weights, w8a8.cu).
 #include <cstring>
 
+#include "decode.h"
 #include "gemv.h"
 #include "skinny.cuh"
 #include "w4a8.h"
@@ -23,10 +24,39 @@ cudaError_t w4a8_launch(const GemvParams &p, int grid, int smem, cudaStream_t st
 
 qmm_status wxa8_dispatch(int bits, const int8_t *xq, const void *sa, const uint8_t *w, const void *ws,
                          int group, void *y, int32_t *acc_out, int M, int N, int K, int *status,
-                         int num_sms, int smem_optin, int smem_pair, cudaStream_t stream)
+                         int num_sms, int smem_optin, int smem_pair, bool allow_decode, cudaStream_t stream)
 {
-    if (M >= (bits == 8 ? kW8a8TcMinM : kW4a8TcMinM) && wxa8_tc_takes(bits, M, N, K, group, xq, w))
+    DecodePlan plan;
+    const bool decode = allow_decode && M <= kWxa8DecodeMaxM && reinterpret_cast<uintptr_t>(w) % 16 == 0 &&
+                        reinterpret_cast<uintptr_t>(xq) % 16 == 0 &&
+                        decode_plan(M, N, K, group, bits, false, false, num_sms, smem_pair, smem_optin, &plan);
+    const int tc_min = decode ? kWxa8DecodeMaxM + 1 : bits == 8 ? kW8a8TcMinM : kW4a8TcMinM;
+    if (M >= tc_min && wxa8_tc_takes(bits, M, N, K, group, xq, w))
         return wxa8_tc_dispatch(bits, xq, sa, w, ws, group, y, acc_out, M, N, K, status, smem_optin, stream);
+    if (decode) {
+        // the decode kernel's exact-integer mode: weights staged before the
+        // dependency wait, codes as exact small integers on the tensor cores
+        DecodeParams d;
+        std::memset(&d, 0, sizeof(d));
+        d.x = reinterpret_cast<const uint16_t *>(xq);
+        d.packed = w;
+        d.scales = static_cast<const uint16_t *>(ws);
+        d.zeros = nullptr;
+        d.y = y;
+        d.status = status;
+        d.row_bytes = static_cast<long long>(K) * bits / 8;
+        d.M = M;
+        d.N = N;
+        d.K = K;
+        d.group_log2 = group == 64 ? 6 : 7;
+        d.zero_const = 1 << (bits - 1);
+        d.vec_sz = reinterpret_cast<uintptr_t>(ws) % 16 == 0;
+        d.sa = static_cast<const uint16_t *>(sa);
+        d.acc_out = acc_out;
+        d.pl = plan;
+        decode_set_tma(d);
+        return launch_decode_int(d, bits, stream) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+    }
     GemvParams p;
     std::memset(&p, 0, sizeof(p));
     p.xq = xq;

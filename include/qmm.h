@@ -137,7 +137,8 @@ QMM_API qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *pac
 /* Kernel choice of qmm_gemv for the calls that follow, process-wide:
  *   QMM_GEMV_AUTO   (0, the default) the decode kernel where it applies,
  *                   else the skinny kernel;
- *   QMM_GEMV_SKINNY (1) the skinny kernel for every shape.
+ *   QMM_GEMV_SKINNY (1) the skinny kernel for every shape (and qmm_w4a8 /
+ *                   qmm_w8a8 off the decode kernel: the skinny or tcgen05 one).
  * Returns QMM_ERR_SHAPE for any other value.  The setting is read when a call
  * is issued; it does not change calls already issued. */
 typedef enum { QMM_GEMV_AUTO = 0, QMM_GEMV_SKINNY = 1 } qmm_gemv_kernel;
@@ -181,12 +182,16 @@ QMM_API qmm_status qmm_gemm(const void *x, qmm_dtype x_dtype, const uint8_t *pac
  *   y       (device) fp16 [M][N].
  *   acc_out (device, may be NULL) int32 [M][N][K/G]: the integer accumulators.
  * Requires 1 <= M <= 64 (decode and small batches), K % G == 0.
- * Two kernels serve it.  For M >= 6 with K a multiple of 512 and K/G/4 <= 32
- * (and xq, w4 16-byte aligned) a tcgen05 kernel runs: weights and activations
- * become exact fp16 operands, each group accumulates in its own tensor-memory
- * accumulator (every product and sum is an integer below 2^24, so the fp32
- * accumulation is exact), and a cluster of four CTAs splits K.  Other shapes
- * take the skinny kernel (fp16 mma.sync on the same exact operands). */
+ * Three kernels serve it, all on exact fp16 operands (every product and group
+ * sum is an integer below 2^24, so fp32 accumulation is exact).  Up to M = 8,
+ * with G in {64, 128}, K % (8*G) == 0 and xq, w4 16-byte aligned, the decode
+ * kernel of qmm_gemv in its exact-integer mode (weights staged in shared
+ * memory before the dependency wait).  Above that, and from M = 6 where the
+ * decode kernel does not apply, a tcgen05 kernel when K is a multiple of 512
+ * and K/G/4 <= 32: each group accumulates in its own tensor-memory
+ * accumulator, a cluster of four CTAs splits K.  Every other shape takes the
+ * skinny kernel (mma.sync).  qmm_set_gemv_kernel(QMM_GEMV_SKINNY) keeps this
+ * call (and qmm_w8a8) off the decode kernel. */
 QMM_API qmm_status qmm_w4a8(const int8_t *xq, const void *sa, const uint8_t *w4, const void *ws,
                     int group, void *y, int32_t *acc_out, int M, int N, int K,
                     cudaStream_t stream);
@@ -278,9 +283,10 @@ QMM_API qmm_status qmm_flip_sign(uint8_t *packed, int N, int K, int bits, cudaSt
  *        aligned.  Everything else as for qmm_w4a8:
  *   acc[m][n][g] = sum_{k in g} xq[m][k] * w8[n][k]   (exact int32)
  *   y[m][n]      = sa[m] * sum_g ws[n][g] * acc[m][n][g]   (fp32 -> fp16 RNE)
- * 1 <= M <= 64, G in {32, 64, 128}.  Errors as for qmm_w4a8.  The tcgen05
- * kernel of qmm_w4a8 serves M >= 2 under the same conditions on K (|acc| <=
- * 128 * 128 * G stays exact), the skinny kernel the rest. */
+ * 1 <= M <= 64, G in {32, 64, 128}.  Errors as for qmm_w4a8.  The kernels
+ * and their conditions are qmm_w4a8's (|acc| <= 128 * 128 * G stays exact),
+ * except that the tcgen05 kernel starts at M = 2 where the decode kernel does
+ * not apply. */
 QMM_API qmm_status qmm_w8a8(const int8_t *xq, const void *sa, const int8_t *w8, const void *ws,
                             int group, void *y, int32_t *acc_out, int M, int N, int K,
                             cudaStream_t stream);
