@@ -12,7 +12,12 @@
 // depends only on the position of code k in its run.  Every product is exact
 // in fp32; mma.sync accumulates a group in fp32, and the group's offset C, zero
 // and scale are applied in fp32 afterwards.  C and X are summed in fp32 when
-// the activations are staged, so no per-code subtraction is needed.
+// the activations are staged, so no per-code subtraction is needed.  Two
+// variants share the kernel: float weight codes (FL: the code's fields placed
+// in an fp16 number, no offset), and the exact-integer mode of qmm_w4a8 /
+// qmm_w8a8 (IX: int8 activations, signed codes read as offset binary, the
+// offset 2^E taken off each operand so that every group sum is an exact
+// integer in fp32, y = sa[m] * sum_g s (acc - 2^(b-1) X)).
 //
 // Staging.  The weights are the one large operand and are never the output of
 // the preceding kernel, so every CTA copies its share of them into shared
@@ -26,8 +31,9 @@
 // Work split.  CTA c owns consecutive output columns (rows of the packed
 // matrix), taken in row blocks of at most 32 (two 16-row MMA tiles).  A row
 // block's K range is cut into segments of 8 groups; one segment of one row
-// block fills one slot of a ring in shared memory (one bulk copy per row, rows
-// at a padded pitch that keeps the fragment reads free of bank conflicts).
+// block fills one slot of a ring in shared memory (one tensor-map copy of the
+// slot's rows, or one bulk copy per row where the pitch is too wide for a box;
+// rows at a padded pitch that keeps the fragment reads free of bank conflicts).
 // Warp w owns group w of every segment, in 64-code blocks.  In a block, quad
 // thread t owns the run of codes [16t, 16t + 16) of each of its four rows; the
 // plan pairs the run's codes, and the MMA's k order follows the pairing (the
@@ -268,7 +274,8 @@ __device__ __forceinline__ void block_mma(const uint8_t *const (&run0)[2][2], in
 // Stores one 16-code run of activations (in[8] = its 16 fp16 values in code
 // order) in fragment (slot) order: slot s of the run holds x of the run's code
 // code_of_slot(s).  Returns the run's sums X = sum x and C = sum 2^E x (E of
-// each code's position in the plan), in fp32.
+// each code's position in the plan; 0 for float codes and the exact-integer
+// mode), in fp32.  IX: raw[0] holds 16 int8 activations instead.
 template <int B, bool FL, bool IX = false>
 __device__ __forceinline__ float2 stage_run(uint8_t *dst, const uint4 (&raw)[2], bool x_bf16)
 {
