@@ -122,10 +122,11 @@ QMM_API qmm_status qmm_unpack(const uint8_t *packed, uint8_t *codes, int N, int 
  * Two kernels serve the call (qmm_gemv_route() tells which).  The decode kernel
  * takes G in {64, 128}, K % (8*G) == 0 and a 16-byte aligned `packed` when its
  * planner finds a shared-memory layout: each CTA copies its weight rows into
- * shared memory before waiting on the preceding kernel (one bulk copy per row,
- * or one 2-D tensor copy per 16 rows when its ring holds one K segment per
- * slot), then stages the activations.  The skinny kernel takes every other shape (fp16 activations
- * only: QMM_BF16 there returns QMM_ERR_UNSUPPORTED); M x K fp16 must fit in
+ * shared memory before waiting on the preceding kernel (one 2-D tensor copy
+ * per ring slot, or one bulk copy per row where a slot's row pitch exceeds
+ * 2048 bytes), then stages the activations.  The skinny kernel takes every
+ * other shape (fp16 activations only: QMM_BF16 there returns
+ * QMM_ERR_UNSUPPORTED); M x K fp16 must fit in
  * its shared memory next to the weight pipeline (larger return
  * QMM_ERR_UNSUPPORTED).  The two sum in different orders, so their outputs may
  * differ in the last bits.  qmm_set_gemv_kernel() forces the skinny kernel.
