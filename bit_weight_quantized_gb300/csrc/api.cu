@@ -159,6 +159,16 @@ bool encode_u64_tmap(CUtensorMap *map, const void *base, long long cols, long lo
     return r == CUDA_SUCCESS;
 }
 
+void skinny_set_tma(GemvParams &p)
+{
+    p.tma = 0;
+    if (p.use_bulk && p.pitch % 16 == 0 && p.pitch > 0 && p.pitch <= 2048 && p.row_bytes % 16 == 0 &&
+        p.seg_bytes % 16 == 0 && p.rb >= 1 && p.rb <= 256 &&
+        static_cast<long long>(p.stage_bytes) >= static_cast<long long>(p.rb) * p.pitch &&
+        encode_u64_tmap(&p.tmw, p.packed, p.row_bytes / 8, p.N, p.pitch / 8, p.rb))
+        p.tma = 1;
+}
+
 // Shared checks of qmm_gemv / qmm_gemm (everything that needs no device).
 static qmm_status check_qmm_args(const void *x, const uint8_t *packed, int bits, int group,
                                  const void *scales, int zero_const, const uint8_t *zeros,
@@ -387,6 +397,7 @@ qmm_status qmm_gemv(const void *x, qmm_dtype x_dtype, const uint8_t *packed, int
     if (st != QMM_OK)
         return st;
     p.use_bulk = aligned(packed, 16) && p.row_bytes % 16 == 0;
+    skinny_set_tma(p);
     cudaError_t e;
     switch (bits) {
     case 1: e = gemv_launch_w1(p, grid, smem, stream); break;

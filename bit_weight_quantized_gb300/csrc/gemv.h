@@ -11,6 +11,10 @@
 namespace qmm {
 
 struct GemvParams {
+    // a 2-D tensor map over the packed weights as 64-bit words [N][row_bytes / 8],
+    // box pitch / 8 words x rb rows, so that one copy lands a stage (tma != 0)
+    alignas(64) CUtensorMap tmw;
+    int tma;
     const uint16_t *x;        // fp16 [M][K]                      (qmm_gemv)
     const int8_t *xq;         // int8 [M][K]                      (qmm_w4a8)
     const uint16_t *sa;       // fp16 [M] per-token scales        (qmm_w4a8)
@@ -39,6 +43,11 @@ struct GemvParams {
     int sz_compact;           // scales staged as fp16 + uint8 zeros (M > 8), else float2 (s, z*s)
     int red_alias;            // the reduction buffer reuses the activation buffer
 };
+
+// Sets p.tma and p.tmw after skinny_plan when a stage can land with one tensor
+// copy: bulk-copyable rows, a pitch that is a whole number of 16-byte units of
+// at most 2048 bytes, segments on 16 bytes and a stage of rb rows.
+void skinny_set_tma(GemvParams &p);
 
 // Chooses grid, row blocking, K phases and the shared-memory layout.  A layout
 // of at most `smem_pair` bytes (two CTAs per SM, so that consecutive calls

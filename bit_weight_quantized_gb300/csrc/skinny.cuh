@@ -329,8 +329,11 @@ static __device__ __noinline__ void stage_scales(const GemvParams &p, uint8_t *s
 }
 
 // Issues pipeline stage `it` (K segment s of row block blk) into ring slot
-// `slot`: one bulk copy per row, completing on full[slot].  Called by a whole
-// warp.  Without 16-byte aligned rows the warp copies with 4-byte loads.
+// `slot`, completing on full[slot]: one tensor copy of rb rows x pitch bytes
+// (p.tma; bytes past a row's end arrive as zeros, rows past the CTA's are the
+// next CTA's or zeros and are not used), else one bulk copy per row.  Called
+// by a whole warp.  Without 16-byte aligned rows the warp copies with 4-byte
+// loads.
 static __device__ __noinline__ void issue_stage(const GemvParams &p, int it, int slot, uint8_t *ring,
                                             uint64_t *full, int r0, int nrows, uint64_t policy)
 {
@@ -343,7 +346,13 @@ static __device__ __noinline__ void issue_stage(const GemvParams &p, int it, int
     const int seg_len = static_cast<int>(min(static_cast<long long>(p.seg_bytes), p.row_bytes - seg_off));
     uint8_t *dst = ring + static_cast<size_t>(slot) * p.stage_bytes;
     const uint8_t *src = p.packed + static_cast<long long>(row0) * p.row_bytes + seg_off;
-    if (p.use_bulk) {
+    if (p.tma && (smem_u32(dst) & 127u) == 0) {   // a tensor copy lands on 128 bytes
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(p.rb * p.pitch));
+            tma_load_2d_hint(dst, &p.tmw, &full[slot], static_cast<int>(seg_off >> 3), row0, policy);
+        }
+        __syncwarp();
+    } else if (p.use_bulk) {
         if (lane == 0)
             mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(rows_here * seg_len));
         __syncwarp();
@@ -370,7 +379,7 @@ static __device__ __noinline__ void issue_stage(const GemvParams &p, int it, int
 
 template <int B, int NT, int R, int MODE>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
-skinny_kernel(const GemvParams p)
+skinny_kernel(const __grid_constant__ GemvParams p)
 {
     constexpr int MP = 8 * NT;                 // padded token count of the D fragments
     constexpr int NGC = 128 / (4 * R);         // groups per 128-code chunk

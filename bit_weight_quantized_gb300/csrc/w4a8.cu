@@ -80,6 +80,7 @@ qmm_status wxa8_dispatch(int bits, const int8_t *xq, const void *sa, const uint8
     if (st != QMM_OK)
         return st;
     p.use_bulk = (reinterpret_cast<uintptr_t>(w) % 16 == 0) && (p.row_bytes % 16 == 0);
+    skinny_set_tma(p);
     const cudaError_t e = bits == 8 ? w8a8_launch(p, grid, smem, stream) : w4a8_launch(p, grid, smem, stream);
     return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
 }
