@@ -4,7 +4,10 @@ each group accumulates exactly in its own tensor-memory accumulator, and the
 partial totals meet in distributed shared memory.  The int32 per-group
 accumulators must equal the oracle's bit for bit, the fp16 output must meet
 the benchmark spec's bound, at every group size, ragged N (row tiles of 128 cut by
-N) and the extreme accumulators."""
+N) and the extreme accumulators.  Up to eight tokens the decode kernel's
+exact-integer mode takes the shapes it can (test_gpu_wxa8_decode.py), so this
+module switches that route off (qmm_set_gemv_kernel("skinny")) to keep the
+tcgen05 kernel on every case from 6 (W4A8) / 2 (W8A8) tokens."""
 import numpy as np
 import pytest
 import torch
@@ -20,7 +23,9 @@ pytestmark = pytest.mark.gpu
 def q():
     import bit_weight_quantized_gb300 as q
     q.load()
-    return q
+    q.qmm_set_gemv_kernel("skinny")   # the decode route off: small batches take tcgen05
+    yield q
+    q.qmm_set_gemv_kernel("auto")
 
 
 def _f16(a):
