@@ -205,7 +205,7 @@ def _code_exps(b):
     return e
 
 
-def _emulate_staged(prob, packed, plan, tile16=False):
+def _emulate_staged(prob, packed, plan, tile16=False, ix_sa=None, acc_out=None):
     """y of the staged decode kernel, emulated from its plan: bulk copies place each
     row's chunk in a ring slot at the plan's pitch; each warp stages its group of
     every segment in fragment (slot) order and forms X and C per group; every lane
@@ -213,7 +213,12 @@ def _emulate_staged(prob, packed, plan, tile16=False):
     address formulas (asserting each read stays in its region), extracts its code
     pairs 2^E + q with the generated plan, and the MMA order follows the pairs.
     Products and sums are exact (fp64 over exact fp16 values); the group fold is
-    s (acc - C - z X)."""
+    s (acc - C - z X).  With ix_sa (the per-token scales) it emulates the
+    exact-integer mode instead: prob.x holds the int8 activations as fp16, the
+    words of the signed stream are XORed to offset binary before extraction and
+    each operand loses its 2^E, C = 0, and the accumulators acc - z X go to
+    acc_out[m][n][g]; y is scaled by ix_sa[m]."""
+    ix = ix_sa is not None
     b, M, N, K, G = prob.bits, prob.M, prob.N, prob.K, prob.group
     ng = K // G
     nw = dec_words(b)
@@ -227,6 +232,7 @@ def _emulate_staged(prob, packed, plan, tile16=False):
     xbits = prob.x.view(np.uint16)
     scb = prob.scales.view(np.uint16)
     slot_code = _slot_codes(b)
+    slots, exps = slot_code, _code_exps(b)
     y = np.zeros((M, N))
     for cta in range(plan["grid"]):
         u0 = cta * plan["rows_base"] + min(cta, plan["rows_rem"])
@@ -260,7 +266,8 @@ def _emulate_staged(prob, packed, plan, tile16=False):
                             run = xbits[m, src:src + 16]
                             sm[dst:dst + 32] = run[slot_code].view(np.uint8)
                             X[w, m, j] += xf[m, src:src + 16].sum()
-                            C[w, m, j] += (pw * xf[m, src:src + 16]).sum()
+                            if not ix:   # the integer mode's operands carry no offset
+                                C[w, m, j] += (pw * xf[m, src:src + 16]).sum()
         assert plan["off_xsum"] + W * M * nseg * 8 <= plan["off_sc"]   # (X, C) fp32 pairs
         nrb = -(-nrows // 32)
         span = plan["span"]
@@ -330,9 +337,14 @@ def _emulate_staged(prob, packed, plan, tile16=False):
                                         if b == 8:
                                             assert a % 16 == 0
                                         raw = [int(v) for v in sm[a:a + 4 * nw].view("<u4")]
+                                        if ix:   # two's complement -> offset binary
+                                            raw = [v ^ (0x88888888 if b == 4 else 0x80808080) for v in raw]
                                         run = [funnelshift_r(raw[k], raw[k + 1] if k + 1 < nw else 0, o)
                                                if b & 1 else raw[k] for k in range(nw)]
                                         for pi, (qlo, qhi) in enumerate(_plan_pairs(b, run)):
+                                            if ix:   # the plan's offsets come off: the codes themselves
+                                                qlo -= 2.0 ** exps[slots[2 * pi]]
+                                                qhi -= 2.0 ** exps[slots[2 * pi + 1]]
                                             jp, hp = divmod(pi, 2)
                                             A[row, 16 * t + 4 * jp + 2 * hp] = qlo
                                             A[row, 16 * t + 4 * jp + 2 * hp + 1] = qhi
@@ -349,7 +361,11 @@ def _emulate_staged(prob, packed, plan, tile16=False):
                         s = float(np.array([sc[e]], dtype=np.uint16).view(np.float16)[0])
                         z = zo[e] if zo is not None else float(prob.zero_const)
                         tot[w, row] += s * (acc[row] - C[w, :, j] - z * X[w, :, j])
+                        if ix and acc_out is not None and row < cnt:
+                            acc_out[:, r0 + rr + row, gidx] = acc[row] - z * X[w, :, j]
             y[:, r0 + rr:r0 + rr + cnt] = tot.sum(axis=0)[:cnt].T
+    if ix:
+        y = y * np.asarray(ix_sa, dtype=np.float64)[:, None]
     return y
 
 
@@ -422,6 +438,36 @@ def test_staged_kernel_emulation_tma_boxes(b, M, N, K, G, zm, budget, tmp_path):
     y = _emulate_staged(prob, oracle.pack(prob.codes, b)[0], plan)
     ref = oracle.solve_qmm(prob)
     np.testing.assert_allclose(y, ref, rtol=0, atol=1e-9 * max(1.0, np.abs(ref).max()))
+
+
+@pytest.mark.parametrize("b,M,N,K,G,sms", [
+    (4, 1, 40, 1024, 128, 4), (4, 3, 75, 1024, 64, 2), (4, 8, 37, 2048, 128, 1), (4, 5, 20, 512, 64, 1),
+    (8, 1, 33, 1024, 128, 2), (8, 4, 19, 512, 64, 1), (8, 2, 66, 2048, 64, 4)])
+def test_staged_kernel_emulation_integer_mode(b, M, N, K, G, sms, tmp_path):
+    # the exact-integer mode of qmm_w4a8 / qmm_w8a8 (int8 activations, signed
+    # codes as offset binary, the plan's offsets taken off each operand): its
+    # accumulators equal the oracle's integers and its output the oracle's y
+    from types import SimpleNamespace
+    import oracle
+    import synthetic
+    from tests.test_planner import SMEM_OPTIN, SMEM_PAIR, decode_plans
+    if b == 4:
+        prob = synthetic.make_w4a8(M, N, K, G, seed=M * 11 + N)
+        codes = prob.w4
+        y_ref, acc_ref, ov = oracle.solve_w4a8(prob)
+    else:
+        prob = synthetic.make_w8a8(M, N, K, G, seed=M * 13 + N)
+        codes = prob.w8.view(np.uint8)
+        y_ref, acc_ref, ov = oracle.solve_w8a8(prob)
+    assert not ov
+    view = SimpleNamespace(bits=b, M=M, N=N, K=K, group=G, x=prob.xq.astype(np.float16), scales=prob.ws,
+                           zeros=None, zero_const=1 << (b - 1))
+    plan = decode_plans([(M, N, K, G, b, 0, sms, SMEM_PAIR, SMEM_OPTIN)], tmp_path)[0]
+    assert plan is not None
+    acc = np.zeros((M, N, K // G))
+    y = _emulate_staged(view, oracle.pack(codes, b)[0], plan, ix_sa=prob.sa.astype(np.float64), acc_out=acc)
+    np.testing.assert_array_equal(acc, acc_ref.astype(np.float64))
+    np.testing.assert_allclose(y, y_ref, rtol=1e-12, atol=1e-12 * np.abs(y_ref).max())
 
 
 def _float_pair_bits(word, q, b, e, m):
