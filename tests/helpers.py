@@ -4,7 +4,7 @@ import torch
 
 import oracle
 
-# The benchmark spec's tolerance for fp16 outputs: max|y - y_ref| / max|y_ref|.
+# The parity bound for fp16 outputs: max|y - y_ref| / max|y_ref|.
 REL_TOL = 2e-3
 
 

@@ -9,7 +9,7 @@ ends of their range, the largest zero a byte can store, and scales blown up
 until the outputs approach the top of the fp16 range.  Every output is compared
 with the fp64 oracle on the same seeded inputs:
 
-* fp16 outputs: max|y - y_ref| / max|y_ref| <= 2e-3 (the north-star bound);
+* fp16 outputs: max|y - y_ref| / max|y_ref| <= 2e-3 (the parity bound);
 * bf16 outputs: elementwise |y - y_ref| <= 2e-3 max|y_ref| + |y_ref| 2^-8 (the
   bf16 rounding of the output itself is up to half an ulp, 2^-8 relative).
 

@@ -1,6 +1,6 @@
 """GPU parity of the tiled tcgen05 path (qmm_gemm, M >= 17) against the oracle.
 
-fp16 activations/outputs use the benchmark spec's bound max|y - y_ref| / max|y_ref|
+fp16 activations/outputs use the parity bound max|y - y_ref| / max|y_ref|
 <= 2e-3.  bf16 outputs cannot meet that bound by rounding alone (half a bf16
 ulp is up to 2^-8 of an element), so they are checked elementwise against
 2e-3 * max|y_ref| plus the output's own half ulp (|y_ref| * 2^-8) plus six

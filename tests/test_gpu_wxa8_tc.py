@@ -3,7 +3,7 @@ W4A8, 2 .. 64 for W8A8, K a multiple of 512): a cluster of four CTAs splits K,
 each group accumulates exactly in its own tensor-memory accumulator, and the
 partial totals meet in distributed shared memory.  The int32 per-group
 accumulators must equal the oracle's bit for bit, the fp16 output must meet
-the benchmark spec's bound, at every group size, ragged N (row tiles of 128 cut by
+the 2e-3 parity bound, at every group size, ragged N (row tiles of 128 cut by
 N) and the extreme accumulators.  Up to eight tokens the decode kernel's
 exact-integer mode takes the shapes it can (test_gpu_wxa8_decode.py), so this
 module switches that route off (qmm_set_gemv_kernel("skinny")) to keep the
