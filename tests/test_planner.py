@@ -265,3 +265,23 @@ def test_decode_plan_tile16_layout(tmp_path_factory):
     sweep = {sh[4]: pl for sh, pl in zip(shapes, plans) if sh[:4] == (1, 4096, 4096, 128) and sh[6] == 152}
     for b in (1, 3, 4):
         assert sweep[b]["span"] == sweep[b]["nseg"] and sweep[b]["smem"] <= SMEM_PAIR, b
+
+
+def test_stage_tensor_box_fits(plans):
+    # where the skinny kernel lands a stage with one tensor copy (pitch <= 2048
+    # bytes in 16-byte units, 16-byte rows and segments: skinny_set_tma), the box
+    # of rb rows x pitch bytes stays inside its stage, and the stages start on
+    # 128 bytes (the kernel checks this too and falls back to bulk copies)
+    n = 0
+    for p in plans:
+        if p["st"] != 0:
+            continue
+        row_bytes = p["K"] * p["bits"] // 8
+        if p["pitch"] % 16 or p["pitch"] > 2048 or row_bytes % 16 or p["seg_bytes"] % 16:
+            continue
+        n += 1
+        key = (p["M"], p["N"], p["K"], p["bits"], p["group"])
+        assert p["rb"] * p["pitch"] <= p["stage_bytes"], key
+        assert p["off_ring"] % 128 == 0 and p["stage_bytes"] % 128 == 0, key
+        assert p["off_ring"] + p["ring"] * p["stage_bytes"] <= p["smem"], key
+    assert n > 0
